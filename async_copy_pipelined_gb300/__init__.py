@@ -1,0 +1,228 @@
+"""Python binding of the pipelined GEMM C ABI (``include/pipelined_gemm.h``).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library
+``_build/libpipelined_gemm.so``.  PyTorch supplies device memory and streams.
+There is no fallback of any kind: if the library is missing or a call fails,
+an exception says so.
+
+    import torch, async_copy_pipelined_gb300 as pg
+    C = pg.gemm_f32(A, B, fill="tma", stages=4)          # A, B CUDA float32
+    C = pg.gemm_bf16(Ab, Bb)                              # A, B CUDA bfloat16
+    C = pg.gemm_f32(A_cpu, B_cpu, fill="cpasync")         # host tensors: copied in and out
+
+Leading dimensions come from the tensors' row strides, so a padded matrix is
+a column slice of a wider buffer (``buf[:, :K]`` with ``buf.stride(0) == lda``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "FILL", "GemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "plan_f32", "plan_bf16",
+    "device_status", "selftest_bounded_wait", "status_string", "build",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libpipelined_gemm.so")
+
+FILL = {"sync": 0, "cpasync": 1, "tma": 2}
+
+GEMM_OK = 0
+STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_UNSUPPORTED",
+                4: "GEMM_ERR_ARCH", 5: "GEMM_ERR_CUDA", 6: "GEMM_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "fill_mode", "block_m", "block_n", "block_k", "thread_m", "thread_n", "threads", "stages",
+        "a_copy_bytes", "b_copy_bytes", "smem_bytes", "grid_x", "grid_y", "k_slices")]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+def _bind(l):
+    I, P, U = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint)
+    l.gemm_f32.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]
+    l.gemm_f32.restype = I
+    l.gemm_f32_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, ctypes.POINTER(GemmPlan)]
+    l.gemm_f32_plan.restype = I
+    l.gemm_bf16.argtypes = [I, I, I, P, I, P, I, P, I, I, I, P]
+    l.gemm_bf16.restype = I
+    l.gemm_bf16_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, ctypes.POINTER(GemmPlan)]
+    l.gemm_bf16_plan.restype = I
+    l.gemm_status_string.argtypes = [I]
+    l.gemm_status_string.restype = ctypes.c_char_p
+    l.gemm_device_status.argtypes = [P, U]
+    l.gemm_device_status.restype = I
+    l.gemm_selftest_bounded_wait.argtypes = [I, P]
+    l.gemm_selftest_bounded_wait.restype = I
+    l.gemm_version.argtypes = []
+    l.gemm_version.restype = I
+    return l
+
+
+def lib():
+    """The loaded C library (ctypes).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library not built ({_LIB_PATH} missing): run "
+                    "`python -m async_copy_pipelined_gb300.buildlib` or __graft_entry__.build()")
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().gemm_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _fill_code(fill) -> int:
+    if isinstance(fill, str):
+        if fill not in FILL:
+            raise ValueError(f"fill must be one of {sorted(FILL)}")
+        return FILL[fill]
+    return int(fill)
+
+
+def _matrix_args(x, name):
+    """(rows, cols, ld, pointer) of a 2-D tensor whose rows are contiguous."""
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major rows)")
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 1 else max(cols, 1)
+    return rows, cols, max(ld, cols, 1), x.data_ptr()
+
+
+def _check(status: int, what: str):
+    if status != GEMM_OK:
+        raise GemmError(status, what)
+
+
+def plan_f32(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_tile=0,
+             a_ptr=256, b_ptr=256, c_ptr=256) -> dict:
+    """What gemm_f32 would launch for these sizes (no device access)."""
+    p = GemmPlan()
+    st = lib().gemm_f32_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
+                             _fill_code(fill), stages, block_tile, ctypes.byref(p))
+    _check(st, "gemm_f32_plan")
+    return p.as_dict()
+
+
+def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, stages=0, a_ptr=256, b_ptr=256, c_ptr=256) -> dict:
+    p = GemmPlan()
+    st = lib().gemm_bf16_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
+                              FILL["tma"], stages, ctypes.byref(p))
+    _check(st, "gemm_bf16_plan")
+    return p.as_dict()
+
+
+def _host_roundtrip(fn, A, B, C, dtype_out):
+    """Host tensors: pinned H2D copies, the device call, D2H copy of C."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Ad = A.to(dev, non_blocking=True)
+    Bd = B.to(dev, non_blocking=True)
+    Cd = fn(Ad, Bd, None)
+    if C is None:
+        C = torch.empty(Cd.shape, dtype=dtype_out, pin_memory=True)
+    C.copy_(Cd, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return C
+
+
+def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
+    """C = A @ B in float32 through the library's FP32 kernel with the given fill.
+
+    A (M x K), B (K x N) float32 tensors; C (M x N) float32 output, allocated
+    if None.  CUDA tensors run on the device asynchronously on `stream`
+    (default: torch's current stream).  CPU tensors are copied to the current
+    device, computed, and copied back (the end-to-end path).
+    """
+    import torch
+    if not A.is_cuda:
+        return _host_roundtrip(lambda a, b, _c: gemm_f32(a, b, None, fill=fill, stages=stages,
+                                                         block_tile=block_tile, stream=stream),
+                               A, B, C, torch.float32)
+    if A.dtype != torch.float32 or B.dtype != torch.float32:
+        raise TypeError("gemm_f32 takes float32 tensors")
+    M, K, lda, pa = _matrix_args(A, "A")
+    K2, N, ldb, pb = _matrix_args(B, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    Mc, Nc, ldc, pc = _matrix_args(C, "C")
+    if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
+        raise ValueError("C must be a float32 M x N tensor")
+    st = lib().gemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_tile,
+                        _stream_handle(stream))
+    _check(st, "gemm_f32")
+    return C
+
+
+def gemm_bf16(A, B, C=None, *, stages=0, stream=None):
+    """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores."""
+    import torch
+    if not A.is_cuda:
+        return _host_roundtrip(lambda a, b, _c: gemm_bf16(a, b, None, stages=stages, stream=stream),
+                               A, B, C, torch.float32)
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("gemm_bf16 takes bfloat16 tensors")
+    M, K, lda, pa = _matrix_args(A, "A")
+    K2, N, ldb, pb = _matrix_args(B, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    Mc, Nc, ldc, pc = _matrix_args(C, "C")
+    if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
+        raise ValueError("C must be a float32 M x N tensor")
+    st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, FILL["tma"], stages, _stream_handle(stream))
+    _check(st, "gemm_bf16")
+    return C
+
+
+def device_status(stream=None):
+    """(status, detail word) after synchronising `stream`; clears the word."""
+    detail = ctypes.c_uint(0)
+    st = lib().gemm_device_status(_stream_handle(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def selftest_bounded_wait(timeout_us: int, stream=None) -> int:
+    return lib().gemm_selftest_bounded_wait(int(timeout_us), _stream_handle(stream))

@@ -1,0 +1,434 @@
+// C ABI of the pipelined GEMM library: argument validation, launch planning,
+// the device status word, TMA tensor-map encoding and the bounded-wait
+// self-test.  Everything here runs on the host except the two tiny kernels at
+// the bottom.
+//
+// Validation mirrors the lesson program's gates ("pipelined_gemm.cu", main:
+// refuse an unsuitable device before doing anything, check every result
+// before timing) but reports a status code instead of exiting.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+#include "tma_ring.cuh"
+
+namespace pg {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull; // 2 s
+constexpr int kDefaultStagesCpAsync = 3;
+constexpr int kDefaultStagesTma = 4;
+constexpr int kDefaultStagesBf16 = 4;
+constexpr int kMaxStagesBf16 = 4;
+// Two resident 128x128 CTAs per SM on a 152-SM GB300: below this many
+// 128x128 tiles the 64x64 tile gives the better-filled grid.
+constexpr long long kLargeTileMinTiles = 304;
+
+__device__ unsigned int g_status_word;
+
+// ------------------------------------------------------------ device state
+static std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 ok, 2 wrong arch
+static std::atomic<uintptr_t> g_status_ptr[kMaxDevices];
+static std::atomic<int> g_num_sms[kMaxDevices];
+
+static int current_device(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+// The kernels are built for sm_103a only; refuse anything else up front
+// rather than launching code that cannot run there.
+static int check_device(int *dev_out)
+{
+    int dev;
+    if (current_device(&dev) != GEMM_OK)
+        return GEMM_ERR_CUDA;
+    int state = g_arch_ok[dev].load();
+    if (state == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_num_sms[dev].store(sms);
+        g_arch_ok[dev].store(state);
+    }
+    if (state != 1)
+        return GEMM_ERR_ARCH;
+    *dev_out = dev;
+    return GEMM_OK;
+}
+
+// Address of this library's status word on device `dev` (the current one).
+static unsigned int *status_word(int dev)
+{
+    uintptr_t p = g_status_ptr[dev].load();
+    if (p == 0) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess)
+            return nullptr;
+        p = reinterpret_cast<uintptr_t>(addr);
+        g_status_ptr[dev].store(p);
+    }
+    return reinterpret_cast<unsigned int *>(p);
+}
+
+// ------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uint64_t cols, uint64_t rows,
+                         uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, int swizzle_128b)
+{
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (pitch_bytes & 15u) != 0)
+        return GEMM_ERR_MISALIGNED;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+    if (!encode)
+        return GEMM_ERR_CUDA;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(static_cast<CUtensorMap *>(map_out),
+                              dtype_is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ sizes
+int f32_threads(int tile, int fill)
+{
+    (void)tile;
+    return 256 + (fill == GEMM_FILL_TMA ? 32 : 0);
+}
+
+int f32_smem_bytes(int tile, int fill, int stages)
+{
+    const int stage_bytes = (tile * 16 + 16 * tile) * 4;
+    if (fill == GEMM_FILL_SYNC)
+        return stage_bytes;
+    if (fill == GEMM_FILL_CPASYNC)
+        return stages * stage_bytes;
+    return stages * stage_bytes + 16 * stages + 1024; // + barriers + alignment slack
+}
+
+int bf16_threads() { return 192; }
+
+int bf16_smem_bytes(int stages)
+{
+    const int stage_bytes = (kBf16BlockM * kBf16BlockK + kBf16BlockK * kBf16BlockN) * 2;
+    return stages * stage_bytes + 1024 /* barriers, TMEM slot */ + 1024 /* alignment slack */;
+}
+
+// ------------------------------------------------------------ planning
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                    int fill, int stages, int tile, gemm_plan *plan, F32Args *args)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA)
+        return GEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return GEMM_ERR_INVALID_ARG;
+    const bool work = M > 0 && N > 0;
+    if (work && (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))))
+        return GEMM_ERR_INVALID_ARG;
+    if (!aligned4(A) || !aligned4(B) || !aligned4(C))
+        return GEMM_ERR_MISALIGNED;
+    if (fill == GEMM_FILL_SYNC) {
+        if (stages != 0 && stages != 1)
+            return GEMM_ERR_INVALID_ARG;
+        stages = 1;
+    } else {
+        if (stages == 0)
+            stages = fill == GEMM_FILL_TMA ? kDefaultStagesTma : kDefaultStagesCpAsync;
+        if (stages < 2 || stages > 6)
+            return GEMM_ERR_INVALID_ARG;
+    }
+    if (tile == 0) {
+        const long long t128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
+        tile = t128 >= kLargeTileMinTiles ? 128 : 64;
+    } else if (tile != 64 && tile != 128) {
+        return GEMM_ERR_INVALID_ARG;
+    }
+    const bool a_vec = aligned16(A) && (lda % 4) == 0;
+    const bool b_vec = aligned16(B) && (ldb % 4) == 0;
+    const bool c_vec = aligned16(C) && (ldc % 4) == 0;
+    if (fill == GEMM_FILL_TMA && K > 0 && work && (!a_vec || !b_vec))
+        return GEMM_ERR_MISALIGNED;
+    const long long grid_y = (M + tile - 1) / tile;
+    const long long grid_x = (N + tile - 1) / tile;
+    if (grid_y > 65535 || grid_x > 0x7fffffffLL)
+        return GEMM_ERR_INVALID_ARG;
+
+    if (plan) {
+        std::memset(plan, 0, sizeof *plan);
+        plan->fill_mode = fill;
+        plan->block_m = tile;
+        plan->block_n = tile;
+        plan->block_k = 16;
+        plan->thread_m = tile == 128 ? 8 : 4;
+        plan->thread_n = tile == 128 ? 8 : 4;
+        plan->threads = f32_threads(tile, fill);
+        plan->stages = stages;
+        if (fill == GEMM_FILL_TMA) {
+            plan->a_copy_bytes = tile * 16 * 4;
+            plan->b_copy_bytes = 16 * tile * 4;
+        } else {
+            plan->a_copy_bytes = a_vec ? 16 : 4;
+            plan->b_copy_bytes = b_vec ? 16 : 4;
+        }
+        plan->smem_bytes = f32_smem_bytes(tile, fill, stages);
+        plan->grid_x = static_cast<int>(grid_x);
+        plan->grid_y = static_cast<int>(grid_y);
+        plan->k_slices = (K + 15) / 16;
+    }
+    if (args) {
+        args->M = M;
+        args->N = N;
+        args->K = K;
+        args->A = A;
+        args->lda = lda;
+        args->B = B;
+        args->ldb = ldb;
+        args->C = C;
+        args->ldc = ldc;
+        args->a_vec = a_vec;
+        args->b_vec = b_vec;
+        args->c_vec = c_vec;
+        args->stages = stages;
+        args->tile = tile;
+        args->status = nullptr;
+        args->wait_limit_ns = kDefaultWaitLimitNs;
+    }
+    return GEMM_OK;
+}
+
+static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
+                     int fill, int stages, gemm_plan *plan, Bf16Args *args)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (fill == GEMM_FILL_SYNC || fill == GEMM_FILL_CPASYNC)
+        return GEMM_ERR_UNSUPPORTED;
+    if (fill != GEMM_FILL_TMA)
+        return GEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return GEMM_ERR_INVALID_ARG;
+    const bool work = M > 0 && N > 0;
+    if (work && (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))))
+        return GEMM_ERR_INVALID_ARG;
+    if (stages == 0)
+        stages = kDefaultStagesBf16;
+    if (stages < 2 || stages > kMaxStagesBf16)
+        return GEMM_ERR_INVALID_ARG;
+    if (!aligned4(C))
+        return GEMM_ERR_MISALIGNED;
+    if (work && K > 0 && (!aligned16(A) || !aligned16(B) || (lda % 8) != 0 || (ldb % 8) != 0))
+        return GEMM_ERR_MISALIGNED;
+    const long long tiles_m = (M + kBf16BlockM - 1) / kBf16BlockM;
+    const long long tiles_n = (N + kBf16BlockN - 1) / kBf16BlockN;
+    if (tiles_m * tiles_n > 0x7fffffffLL)
+        return GEMM_ERR_INVALID_ARG;
+    if (plan) {
+        std::memset(plan, 0, sizeof *plan);
+        plan->fill_mode = fill;
+        plan->block_m = kBf16BlockM;
+        plan->block_n = kBf16BlockN;
+        plan->block_k = kBf16BlockK;
+        plan->threads = bf16_threads();
+        plan->stages = stages;
+        plan->a_copy_bytes = kBf16BlockM * kBf16BlockK * 2;
+        plan->b_copy_bytes = kBf16BlockK * 64 * 2;
+        plan->smem_bytes = bf16_smem_bytes(stages);
+        plan->grid_x = static_cast<int>(tiles_m * tiles_n); // upper bound; capped at the SM count on launch
+        plan->grid_y = 1;
+        plan->k_slices = (K + kBf16BlockK - 1) / kBf16BlockK;
+    }
+    if (args) {
+        args->M = M;
+        args->N = N;
+        args->K = K;
+        args->A = A;
+        args->lda = lda;
+        args->B = B;
+        args->ldb = ldb;
+        args->C = C;
+        args->ldc = ldc;
+        args->stages = stages;
+        args->status = nullptr;
+        args->wait_limit_ns = kDefaultWaitLimitNs;
+        args->num_sms = 0;
+    }
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------ self-test kernel
+__global__ void selftest_wait_kernel(unsigned int *status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the wait must expire and report.
+        if (!mbar_wait_bounded(b, 0, limit_ns))
+            record_error(status, kErrFamilySelftest | kErrRoleConsumer);
+    }
+}
+
+int launch_selftest_wait(unsigned int *status, unsigned long long limit_ns, cudaStream_t s)
+{
+    selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+} // namespace pg
+
+using namespace pg;
+
+// ================================================================ C ABI
+extern "C" {
+
+int gemm_version(void) { return 10000; }
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid size, leading dimension, pointer, fill, stages or tile";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: base or row pitch not aligned as the fill requires";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: request not implemented by this build";
+    case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: current device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime or driver call failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel's bounded wait expired";
+    default: return "unknown gemm_status";
+    }
+}
+
+int gemm_f32_plan(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                  int fill_mode, int stages, int block_tile, gemm_plan *plan)
+{
+    if (!plan)
+        return GEMM_ERR_INVALID_ARG;
+    return plan_f32(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_tile, plan, nullptr);
+}
+
+int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc, int fill_mode,
+             int stages, int block_tile, void *stream)
+{
+    F32Args args;
+    int st = plan_f32(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_tile, nullptr, &args);
+    if (st != GEMM_OK)
+        return st;
+    int dev;
+    st = check_device(&dev);
+    if (st != GEMM_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    args.status = status_word(dev);
+    if (!args.status)
+        return GEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return launch_f32_zero(args, s);
+    switch (fill_mode) {
+    case GEMM_FILL_SYNC: return launch_f32_sync(args, s);
+    case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);
+    default: return launch_f32_tma(args, s);
+    }
+}
+
+int gemm_bf16_plan(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
+                   int fill_mode, int stages, gemm_plan *plan)
+{
+    if (!plan)
+        return GEMM_ERR_INVALID_ARG;
+    return plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, plan, nullptr);
+}
+
+int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
+              int fill_mode, int stages, void *stream)
+{
+    Bf16Args args;
+    int st = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, nullptr, &args);
+    if (st != GEMM_OK)
+        return st;
+    int dev;
+    st = check_device(&dev);
+    if (st != GEMM_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    args.status = status_word(dev);
+    if (!args.status)
+        return GEMM_ERR_CUDA;
+    args.num_sms = g_num_sms[dev].load();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return launch_bf16_zero(args, s);
+    return launch_bf16_tma(args, s);
+}
+
+int gemm_device_status(void *stream, unsigned int *detail)
+{
+    int dev;
+    if (current_device(&dev) != GEMM_OK)
+        return GEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int *word = status_word(dev);
+    if (!word)
+        return GEMM_ERR_CUDA;
+    unsigned int value = 0;
+    if (cudaMemcpyAsync(&value, word, sizeof value, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(word, 0, sizeof(unsigned int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (detail)
+        *detail = value;
+    return value == 0 ? GEMM_OK : GEMM_ERR_TIMEOUT;
+}
+
+int gemm_selftest_bounded_wait(int timeout_us, void *stream)
+{
+    if (timeout_us < 1 || timeout_us > 1000000)
+        return GEMM_ERR_INVALID_ARG;
+    int dev;
+    int st = check_device(&dev);
+    if (st != GEMM_OK)
+        return st;
+    unsigned int *word = status_word(dev);
+    if (!word)
+        return GEMM_ERR_CUDA;
+    return launch_selftest_wait(word, static_cast<unsigned long long>(timeout_us) * 1000ull,
+                                static_cast<cudaStream_t>(stream));
+}
+
+} // extern "C"

@@ -1,0 +1,206 @@
+// FP32 register-tiled GEMM: tile shapes, the shared-memory layout every fill
+// writes, the per-thread micro-kernel every fill runs, the guarded chunk
+// loaders and the epilogue.
+//
+// Design source: "pipelined_gemm.cu" (tile shapes, computeTile, the two
+// fills) and "Day 74: Async copies and pipelines", section "Two kernels, one
+// arithmetic": a block tile filled one 16-deep K slice at a time, a micro-tile
+// of C per thread, and one shared inner product so that the fills execute
+// identical floating-point operations in an identical order.
+#pragma once
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+namespace pg {
+
+// Block tile BM x BN, K slice BK = 16, micro-tile TM x TN per thread.
+//
+// Shared-memory layout of one stage (identical for all fills):
+//   A slice: BM rows x 16 floats, row-major [m][k] (64 bytes per row);
+//   B slice: 16 rows x BN floats, row-major [k][n].
+// Global chunk c (16 bytes) of either slice lands at float offset 4*c, so a
+// warp's 32 chunks are 512 contiguous bytes: conflict-free 16-byte stores,
+// and exactly the dense box a TMA copy writes.
+//
+// Thread (tr, tc) = (tid / (BN/TN), tid % (BN/TN)) owns rows tr + i*(BM/TM)
+// and columns g*(BN/(TN/4)) + 4*tc + e.  With these strides a warp's A reads
+// hit two adjacent rows (distinct banks, broadcast within each) and its B
+// reads cover 256 contiguous bytes per 16-byte load: no bank conflicts.
+template <int BM_, int BN_, int TM_, int TN_, int MIN_BLOCKS_, int MIN_BLOCKS_TMA_>
+struct F32Tile {
+    static constexpr int BM = BM_, BN = BN_, BK = 16, TM = TM_, TN = TN_;
+    // Resident CTAs per SM the register budget is sized for.  The TMA fill's
+    // extra producer warp makes 9 warps per CTA; two such CTAs would put 5
+    // warps on one SM sub-partition and cap the 8x8 micro-tile at 96
+    // registers, so the 128-tile TMA kernel runs one CTA per SM instead.
+    static constexpr int kMinBlocks = MIN_BLOCKS_;
+    static constexpr int kMinBlocksTma = MIN_BLOCKS_TMA_;
+    static constexpr int kThreadCols = BN / TN;
+    static constexpr int kThreadRows = BM / TM;
+    static constexpr int kThreads = kThreadCols * kThreadRows;
+    static constexpr int kColGroups = TN / 4;
+    static constexpr int kColGroupStride = BN / kColGroups;
+    static constexpr int kAFloats = BM * BK;
+    static constexpr int kBFloats = BK * BN;
+    static constexpr int kStageFloats = kAFloats + kBFloats;
+    static constexpr int kStageBytes = kStageFloats * 4;
+    static constexpr int kAChunksPerThread = kAFloats / 4 / kThreads;
+    static constexpr int kBChunksPerThread = kBFloats / 4 / kThreads;
+    static constexpr int kBChunksPerRow = BN / 4;
+
+    static_assert(kThreads % 32 == 0, "whole warps");
+    static_assert(TN % 4 == 0 && BN % 4 == 0, "float4 columns");
+    static_assert(kColGroupStride == 4 * kThreadCols, "column groups tile BN exactly");
+    static_assert((kAFloats / 4) % kThreads == 0 && (kBFloats / 4) % kThreads == 0,
+                  "each thread moves whole chunks of both slices");
+};
+
+using TileS = F32Tile<64, 64, 4, 4, 4, 4>;   // the lesson's 64x64x16, 4x4, 256 threads
+using TileL = F32Tile<128, 128, 8, 8, 2, 1>; // 128x128x16, 8x8, 256 threads
+
+// The inner product all fills share ("pipelined_gemm.cu", computeTile):
+// for each k of the slice, ascending, acc[i][j] = fma(a[i][k], b[k][j],
+// acc[i][j]).  A is read as float4 along k (4 k-steps per load), B as float4
+// along n.  Each C element sees exactly one fused multiply-add per k, in
+// ascending k, whichever fill staged the slice.
+template <class T>
+__device__ __forceinline__ void compute_tile(const float *__restrict__ sA, const float *__restrict__ sB, int tr,
+                                             int tc, float (&acc)[T::TM][T::TN])
+{
+#pragma unroll
+    for (int kq = 0; kq < T::BK / 4; ++kq) {
+        float4 a4[T::TM];
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i)
+            a4[i] = *reinterpret_cast<const float4 *>(sA + (tr + i * T::kThreadRows) * T::BK + kq * 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float b[T::TN];
+#pragma unroll
+            for (int g = 0; g < T::kColGroups; ++g) {
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(sB + (kq * 4 + kk) * T::BN + g * T::kColGroupStride + tc * 4);
+                b[4 * g + 0] = v.x;
+                b[4 * g + 1] = v.y;
+                b[4 * g + 2] = v.z;
+                b[4 * g + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i) {
+                const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+#pragma unroll
+                for (int j = 0; j < T::TN; ++j)
+                    acc[i][j] = __fmaf_rn(a, b[j], acc[i][j]);
+            }
+        }
+    }
+}
+
+// Four consecutive elements (r, c..c+3) of an R x C row-major matrix with
+// leading dimension ld, zero outside the matrix.  `vec` means the row pitch
+// and base allow one 16-byte load.
+__device__ __forceinline__ float4 load_chunk_guarded(const float *__restrict__ base, long long ld, int r, int c, int R,
+                                                     int C, bool vec)
+{
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < R && c < C) {
+        const float *p = base + static_cast<long long>(r) * ld + c;
+        if (vec && c + 4 <= C) {
+            v = *reinterpret_cast<const float4 *>(p);
+        } else {
+            v.x = p[0];
+            if (c + 1 < C)
+                v.y = p[1];
+            if (c + 2 < C)
+                v.z = p[2];
+            if (c + 3 < C)
+                v.w = p[3];
+        }
+    }
+    return v;
+}
+
+// The same four elements into shared memory at `dst` through cp.async.
+// Aligned rows: one 16-byte cp.async.cg whose source size (0, 4, 8, 12 or 16
+// bytes) zero-fills whatever lies outside the matrix.  Unaligned rows: four
+// 4-byte cp.async.ca with source size 4 or 0.  A zero-size copy still names a
+// valid address (the matrix base), never a skipped issue: a predicated-off
+// cp.async would leave stale data instead of zeros ("cp.async", section
+// "Predication is different from zero fill").
+__device__ __forceinline__ void cp_chunk_guarded(uint32_t dst, const float *__restrict__ base, long long ld, int r,
+                                                 int c, int R, int C, bool vec)
+{
+    const bool row_ok = r < R;
+    if (vec) {
+        uint32_t nbytes = 0;
+        const float *src = base;
+        if (row_ok && c < C) {
+            nbytes = static_cast<uint32_t>(min(C - c, 4)) * 4u;
+            src = base + static_cast<long long>(r) * ld + c;
+        }
+        cp_async_cg16(dst, src, nbytes);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool ok = row_ok && (c + e) < C;
+            const float *src = ok ? base + static_cast<long long>(r) * ld + c + e : base;
+            cp_async_ca4(dst + 4u * e, src, ok ? 4u : 0u);
+        }
+    }
+}
+
+// Chunk c of the A slice: row c/4, k offset 4*(c%4).  Of the B slice: row
+// c/(BN/4), n offset 4*(c%(BN/4)).  Both land at float offset 4*c.
+template <class T>
+__device__ __forceinline__ void a_chunk_coords(int c, int m0, int k0, int &r, int &k)
+{
+    r = m0 + c / 4;
+    k = k0 + (c % 4) * 4;
+}
+
+template <class T>
+__device__ __forceinline__ void b_chunk_coords(int c, int k0, int n0, int &k, int &n)
+{
+    k = k0 + c / T::kBChunksPerRow;
+    n = n0 + (c % T::kBChunksPerRow) * 4;
+}
+
+// Write the micro-tile; rows >= M and columns >= N are skipped.
+template <class T>
+__device__ __forceinline__ void store_tile(const F32Args &p, int m0, int n0, int tr, int tc,
+                                           const float (&acc)[T::TM][T::TN])
+{
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i) {
+        const int row = m0 + tr + i * T::kThreadRows;
+        if (row >= p.M)
+            continue;
+        float *crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll
+        for (int g = 0; g < T::kColGroups; ++g) {
+            const int col = n0 + g * T::kColGroupStride + tc * 4;
+            if (p.c_vec && col + 4 <= p.N) {
+                *reinterpret_cast<float4 *>(crow + col) =
+                    make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2], acc[i][4 * g + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < p.N)
+                        crow[col + e] = acc[i][4 * g + e];
+            }
+        }
+    }
+}
+
+template <class T>
+__device__ __forceinline__ void zero_acc(float (&acc)[T::TM][T::TN])
+{
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < T::TN; ++j)
+            acc[i][j] = 0.0f;
+}
+
+} // namespace pg

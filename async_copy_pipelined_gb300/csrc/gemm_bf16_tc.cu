@@ -1,0 +1,315 @@
+// BF16 -> FP32 GEMM on the 5th-generation tensor cores, fed by the same TMA
+// ring as the FP32 TMA fill.
+//
+// The pages' tensor-core loop ("异步拷贝与现代 Pipeline", section 6.1
+// "BF16 GEMM 的异步拷贝": prefetch the next K tile, commit, compute the current
+// tile on the tensor cores, wait, barrier) re-designed for sm_103a:
+//
+//   warp 0      TMA producer: per 64-deep K block, one 128 x 64 box of A and
+//               four 64 x 64 boxes of B (128-byte swizzle) into ring stage
+//               f % S, announced on full[f % S].
+//   warp 1      allocates tensor memory (512 columns: two 128 x 256 FP32
+//               accumulators) and, from one thread, issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M 128, N 256, K 16; four
+//               per K block); tcgen05.commit releases each ring stage to the
+//               producer once its MMAs have read it, and marks an
+//               accumulator full after a tile's last K block.
+//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (each warp
+//               its 32-lane quarter of tensor memory), FP32 stores to C, then
+//               hand the accumulator back.  With two accumulators the
+//               epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ... in
+// groups of 16 M-tiles so the tiles in flight share A and B rows in L2.
+// Ragged M, N, K: TMA zero-fills out-of-range box elements (zeros add nothing
+// to the products) and the epilogue guards its stores.
+//
+// Layouts (PTX ISA shared-memory matrix descriptors, 128-byte swizzle):
+//   A stage  128 rows (m) x 128 bytes (64 k), K-major; 8-row groups 1024 B
+//            apart (SBO); the K step of 16 elements advances 32 bytes.
+//   B stage  four 64(n) x 64(k) boxes, each 64 rows (k) of 128 bytes (64 n):
+//            N-major ("MN-major"); 64-column atoms 8192 B apart (LBO), 8-row K
+//            groups 1024 B apart (SBO); the K step advances 16 rows = 2048 B.
+#include "gemm_internal.h"
+#include "ptx.cuh"
+#include "tma_ring.cuh"
+
+namespace pg {
+
+namespace bf16 {
+constexpr int BM = kBf16BlockM;
+constexpr int BN = kBf16BlockN;
+constexpr int BK = kBf16BlockK;
+constexpr int kUmmaK = 16;
+constexpr uint32_t kATileBytes = BM * BK * 2;             // 16 KiB
+constexpr uint32_t kBBoxCols = 64;                         // n per B box (128 bytes)
+constexpr uint32_t kBBoxBytes = kBBoxCols * BK * 2;        // 8 KiB
+constexpr uint32_t kBTileBytes = BN * BK * 2;              // 32 KiB
+constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 KiB
+constexpr uint32_t kTmemCols = 2 * BN;                     // two accumulators
+constexpr int kGroupM = 16;
+constexpr int kThreads = 192;
+
+// Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = BF16
+// (bits 7-9 = 1), B = BF16 (bits 10-12 = 1), A K-major (bit 15 = 0), B
+// MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
+// byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), descriptor
+// version 1 (46-47), base offset 0 (atoms are 1024-byte aligned), swizzle
+// mode 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb)
+{
+    const int per_group = kGroupM * tiles_n;
+    const int group = t / per_group;
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, tiles_m - first_m);
+    const int r = t - group * per_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+} // namespace bf16
+
+template <int S>
+__global__ void __launch_bounds__(bf16::kThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                        const Bf16Args p)
+{
+    using namespace bf16;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align_smem(raw, 1024);
+    const uint32_t bars = base + S * kStageBytes;
+    const TmaRing<S> ring{bars, bars + 8u * S};
+    const uint32_t tmem_full0 = bars + 16u * S; // [2]
+    const uint32_t tmem_empty0 = tmem_full0 + 16u; // [2]
+    const uint32_t epi_done = tmem_empty0 + 16u;
+    const uint32_t mma_done = epi_done + 8u;
+    const uint32_t tmem_slot = mma_done + 8u;
+    volatile uint32_t *tmem_slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int tiles_m = (p.M + BM - 1) / BM;
+    const int tiles_n = (p.N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int k_blocks = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        ring.init(1);
+        mbar_init(tmem_full0, 1);
+        mbar_init(tmem_full0 + 8u, 1);
+        mbar_init(tmem_empty0, 4);
+        mbar_init(tmem_empty0 + 8u, 4);
+        mbar_init(epi_done, 4);
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_map(&map_a);
+            tma_prefetch_map(&map_b);
+            int f = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, tiles_m, tiles_n, mb, nb);
+                for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                    if (!ring.producer_acquire(f, p.wait_limit_ns)) {
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleProducer);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
+                    const uint32_t full = ring.full_bar(f);
+                    ring.producer_commit(f, kStageBytes);
+                    tma_load_2d(dst, &map_a, full, kb * BK, mb * BM);
+#pragma unroll
+                    for (int j = 0; j < BN / static_cast<int>(kBBoxCols); ++j)
+                        tma_load_2d(dst + kATileBytes + j * kBBoxBytes, &map_b, full,
+                                    nb * BN + j * static_cast<int>(kBBoxCols), kb * BK);
+                }
+            }
+            for (int g = f > S ? f - S : 0; g < f; ++g) {
+                if (!ring.consumer_wait(g, p.wait_limit_ns)) {
+                    record_error(p.status, kErrFamilyBf16 | kErrRoleDrain);
+                    break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int f = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+                const int slot = local & 1;
+                const uint32_t use_parity = static_cast<uint32_t>((local >> 1) & 1);
+                if (!mbar_wait_bounded(tmem_empty0 + 8u * slot, use_parity ^ 1u, p.wait_limit_ns)) {
+                    record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
+                for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                    if (!ring.consumer_wait(f, p.wait_limit_ns)) {
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = base + static_cast<uint32_t>(f % S) * kStageBytes;
+                    const uint32_t b_addr = a_addr + kATileBytes;
+#pragma unroll
+                    for (int ks = 0; ks < BK / kUmmaK; ++ks) {
+                        const uint64_t adesc = smem_desc_sw128(a_addr + ks * kUmmaK * 2, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b_addr + ks * kUmmaK * 128, kBBoxBytes, 1024);
+                        mma_f16_ss(d_tmem, adesc, bdesc, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(ring.empty_bar(f)); // stage free once these MMAs have read it
+                }
+                if (!ok)
+                    break;
+                mma_commit(tmem_full0 + 8u * slot); // accumulator complete
+            }
+            // Every MMA this thread issued must finish before tensor memory is freed.
+            mma_commit(mma_done);
+            if (!mbar_wait_bounded(mma_done, 0, p.wait_limit_ns))
+                record_error(p.status, kErrFamilyBf16 | kErrRoleDrain);
+        }
+        __syncwarp();
+        if (!mbar_wait_bounded(epi_done, 0, p.wait_limit_ns) && lane == 0)
+            record_error(p.status, kErrFamilyBf16 | kErrRoleDrain);
+        tc_fence_after_sync();
+        __syncwarp();
+        tmem_dealloc(tmem_base, kTmemCols);
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int quarter = warp & 3; // tensor-memory lanes 32*quarter .. +31
+        const bool c_vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
+        int local = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+            const int slot = local & 1;
+            const uint32_t use_parity = static_cast<uint32_t>((local >> 1) & 1);
+            const bool ok = mbar_wait_bounded(tmem_full0 + 8u * slot, use_parity, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0)
+                    record_error(p.status, kErrFamilyBf16 | kErrRoleEpilogue);
+                break;
+            }
+            tc_fence_after_sync();
+            int mb, nb;
+            tile_coords(t, tiles_m, tiles_n, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(slot * BN);
+            float *crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N)
+                    break; // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), r);
+                tmem_ld_wait();
+                if (row < p.M) {
+                    if (c_vec && col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(crow + col0 + 4 * j) =
+                                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N)
+                                crow[col0 + j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tmem_empty0 + 8u * slot);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(epi_done);
+    }
+}
+
+__global__ void gemm_bf16_zero_kernel(float *C, int M, int N, long long ldc)
+{
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x)
+        C[(idx / N) * ldc + idx % N] = 0.0f;
+}
+
+template <int S>
+static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
+{
+    using namespace bf16;
+    alignas(64) CUtensorMap map_a;
+    alignas(64) CUtensorMap map_b;
+    int st = encode_tensor_map_2d(&map_a, 1, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                                  static_cast<uint64_t>(a.lda) * 2u, BK, BM, 1);
+    if (st != GEMM_OK)
+        return st;
+    st = encode_tensor_map_2d(&map_b, 1, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.ldb) * 2u, kBBoxCols, BK, 1);
+    if (st != GEMM_OK)
+        return st;
+    const int smem = bf16_smem_bytes(S);
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const long long tiles = static_cast<long long>((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+    const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);
+    gemm_bf16_tc_kernel<S><<<grid, kThreads, smem, s>>>(map_a, map_b, a);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int launch_bf16_tma(const Bf16Args &a, cudaStream_t s)
+{
+    switch (a.stages) {
+    case 2: return launch_bf16_t<2>(a, s);
+    case 3: return launch_bf16_t<3>(a, s);
+    case 4: return launch_bf16_t<4>(a, s);
+    default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int launch_bf16_zero(const Bf16Args &a, cudaStream_t s)
+{
+    const long long total = static_cast<long long>(a.M) * a.N;
+    long long blocks = (total + 255) / 256;
+    blocks = blocks > 4096 ? 4096 : (blocks < 1 ? 1 : blocks);
+    gemm_bf16_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a.C, a.M, a.N, a.ldc);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+} // namespace pg

@@ -1,0 +1,113 @@
+// FP32 GEMM, fill (b): cp.async with commit_group / wait_group completion.
+//
+// Each thread copies its chunks of the slice straight from global to shared
+// memory with cp.async (no register on the way, "Day 74: Async copies and
+// pipelines", section "A copy that skips the registers"), closes them into
+// one commit group per slice, and keeps S-1 slices in flight ahead of the
+// one being computed.  wait_group S-2 returns once at most S-2 of this
+// thread's groups are pending, i.e. once its copies of the slice about to be
+// consumed have landed ("A study on CUDA async memcpy", section
+// "async-group based approach": wait until only the N most recent groups are
+// in flight).  Completion is per thread, so one CTA barrier per slice makes
+// every thread's copies visible to every other thread; the same barrier
+// proves the stage about to be refilled has been consumed by all threads
+// ("Day 74", "Pitfalls": a barrier alone does not wait for copies).
+//
+// The lookahead is the lesson's top-up loop ("pipelined_gemm.cu",
+// matmulTilePiped) with the per-slice acquire/release of its pipeline object
+// replaced by the group count and the barrier.  An empty group is committed
+// past the last slice so the wait count stays uniform.
+#include "f32_tile.cuh"
+
+namespace pg {
+
+template <class T, int S>
+__global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_kernel(const F32Args p)
+{
+    static_assert(S >= 2 && S <= 6, "stages");
+    extern __shared__ __align__(1024) float smem[];
+
+    const int tid = threadIdx.x;
+    const int m0 = blockIdx.y * T::BM;
+    const int n0 = blockIdx.x * T::BN;
+    const int tr = tid / T::kThreadCols;
+    const int tc = tid % T::kThreadCols;
+    const int k_slices = (p.K + T::BK - 1) / T::BK;
+
+    auto issue = [&](int stage, int kt) {
+        float *sA = smem + stage * T::kStageFloats;
+        float *sB = sA + T::kAFloats;
+        const int k0 = kt * T::BK;
+#pragma unroll
+        for (int q = 0; q < T::kAChunksPerThread; ++q) {
+            const int c = tid + q * T::kThreads;
+            int r, k;
+            a_chunk_coords<T>(c, m0, k0, r, k);
+            cp_chunk_guarded(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec);
+        }
+#pragma unroll
+        for (int q = 0; q < T::kBChunksPerThread; ++q) {
+            const int c = tid + q * T::kThreads;
+            int k, n;
+            b_chunk_coords<T>(c, k0, n0, k, n);
+            cp_chunk_guarded(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec);
+        }
+    };
+
+    float acc[T::TM][T::TN];
+    zero_acc<T>(acc);
+
+    // Prologue: slices 0 .. S-2 in flight, one group each.
+#pragma unroll
+    for (int st = 0; st < S - 1; ++st) {
+        if (st < k_slices)
+            issue(st, st);
+        cp_async_commit();
+    }
+
+    for (int kt = 0; kt < k_slices; ++kt) {
+        cp_async_wait<S - 2>(); // this thread's copies of slice kt have landed
+        __syncthreads();        // ... and everyone's; slice kt-1 fully consumed
+        const int fetch = kt + S - 1;
+        if (fetch < k_slices)
+            issue(fetch % S, fetch); // refills the stage slice kt-1 used
+        cp_async_commit();
+        const float *sA = smem + (kt % S) * T::kStageFloats;
+        compute_tile<T>(sA, sA + T::kAFloats, tr, tc, acc);
+    }
+    cp_async_wait<0>();
+
+    store_tile<T>(p, m0, n0, tr, tc, acc);
+}
+
+template <class T, int S>
+static int launch_cpasync_t(const F32Args &a, cudaStream_t s)
+{
+    const int smem = S * T::kStageBytes;
+    if (cudaFuncSetAttribute(gemm_f32_cpasync_kernel<T, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
+    gemm_f32_cpasync_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+template <class T>
+static int launch_cpasync_tile(const F32Args &a, cudaStream_t s)
+{
+    switch (a.stages) {
+    case 2: return launch_cpasync_t<T, 2>(a, s);
+    case 3: return launch_cpasync_t<T, 3>(a, s);
+    case 4: return launch_cpasync_t<T, 4>(a, s);
+    case 5: return launch_cpasync_t<T, 5>(a, s);
+    case 6: return launch_cpasync_t<T, 6>(a, s);
+    default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int launch_f32_cpasync(const F32Args &a, cudaStream_t s)
+{
+    return a.tile == 128 ? launch_cpasync_tile<TileL>(a, s) : launch_cpasync_tile<TileS>(a, s);
+}
+
+} // namespace pg

@@ -1,0 +1,77 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; not part of the public header.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pipelined_gemm.h"
+
+namespace pg {
+
+// One FP32 GEMM request after validation.
+struct F32Args {
+    int M, N, K;
+    const float *A;
+    long long lda;
+    const float *B;
+    long long ldb;
+    float *C;
+    long long ldc;
+    bool a_vec; // A base and row pitch allow 16-byte copies
+    bool b_vec; // same for B
+    bool c_vec; // C base and ldc allow float4 stores
+    int stages;
+    int tile; // 64 or 128
+    unsigned int *status; // device status word
+    unsigned long long wait_limit_ns;
+};
+
+struct Bf16Args {
+    int M, N, K;
+    const uint16_t *A;
+    long long lda;
+    const uint16_t *B;
+    long long ldb;
+    float *C;
+    long long ldc;
+    int stages;
+    unsigned int *status;
+    unsigned long long wait_limit_ns;
+    int num_sms;
+};
+
+// Launchers: each returns a gemm_status.  They assume validated arguments.
+int launch_f32_sync(const F32Args &a, cudaStream_t s);
+int launch_f32_cpasync(const F32Args &a, cudaStream_t s);
+int launch_f32_tma(const F32Args &a, cudaStream_t s);
+int launch_f32_zero(const F32Args &a, cudaStream_t s);
+int launch_bf16_tma(const Bf16Args &a, cudaStream_t s);
+int launch_bf16_zero(const Bf16Args &a, cudaStream_t s);
+int launch_selftest_wait(unsigned int *status, unsigned long long limit_ns, cudaStream_t s);
+
+// Shared-memory bytes the FP32 kernels request for (tile, fill, stages).
+int f32_smem_bytes(int tile, int fill, int stages);
+int f32_threads(int tile, int fill);
+int bf16_smem_bytes(int stages);
+int bf16_threads();
+constexpr int kBf16BlockM = 128;
+constexpr int kBf16BlockN = 256;
+constexpr int kBf16BlockK = 64;
+
+// Encode a 2-D tiled tensor map (row-major rows x cols, pitch in bytes).
+// Returns GEMM_OK or GEMM_ERR_CUDA / GEMM_ERR_MISALIGNED.
+int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uint64_t cols, uint64_t rows,
+                         uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, int swizzle_128b);
+
+// Status codes recorded on device: low byte = kernel family, next byte = role.
+constexpr unsigned int kErrFamilyF32Tma = 1;
+constexpr unsigned int kErrFamilyBf16 = 2;
+constexpr unsigned int kErrFamilySelftest = 3;
+constexpr unsigned int kErrRoleConsumer = 1u << 8;
+constexpr unsigned int kErrRoleProducer = 2u << 8;
+constexpr unsigned int kErrRoleMma = 3u << 8;
+constexpr unsigned int kErrRoleEpilogue = 4u << 8;
+constexpr unsigned int kErrRoleDrain = 5u << 8;
+
+} // namespace pg

@@ -31,6 +31,9 @@ reads them poisons its output) and 0x7FC0 (a bfloat16 NaN) for bfloat16.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -42,17 +45,20 @@ _MASK64 = (1 << 64) - 1
 TAG_A = 1
 TAG_B = 2
 
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
 
 
 def _mix64_array(z: np.ndarray) -> np.ndarray:
-    """SplitMix64 finaliser on a uint64 array (wrap-around arithmetic)."""
-    z = z.copy()
-    z ^= z >> np.uint64(30)
+    """SplitMix64 finaliser on a uint64 array, in place (wrap-around arithmetic)."""
+    t = np.empty_like(z)
+    np.right_shift(z, np.uint64(30), out=t)
+    z ^= t
     z *= _M1
-    z ^= z >> np.uint64(27)
+    np.right_shift(z, np.uint64(27), out=t)
+    z ^= t
     z *= _M2
-    z ^= z >> np.uint64(31)
+    np.right_shift(z, np.uint64(31), out=t)
+    z ^= t
     return z
 
 
@@ -66,17 +72,32 @@ def _mix64_int(x: int) -> int:
 def draws(seed: int, tag: int, start: int, count: int) -> np.ndarray:
     """Raw 64-bit draws ``start .. start+count-1`` of stream (seed, tag)."""
     base = np.uint64(_mix64_int((seed << 32) + tag))
-    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    z = np.arange(start + 1, start + count + 1, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        return _mix64_array(base + idx * _GAMMA)
+        z *= _GAMMA
+        z += base
+    return _mix64_array(z)
 
 
 def _fill_logical(n: int, fn) -> np.ndarray:
-    """Evaluate ``fn(start, count)`` chunk by chunk into one float32 vector."""
+    """Evaluate ``fn(start, count)`` chunk by chunk into one float32 vector.
+
+    Chunks are independent (the stream is counter-based), so they run on a
+    thread pool; numpy releases the GIL inside each operation."""
     out = np.empty(n, dtype=np.float32)
-    for s in range(0, n, _CHUNK):
+    starts = list(range(0, n, _CHUNK))
+
+    def one(s):
         c = min(_CHUNK, n - s)
         out[s:s + c] = fn(s, c)
+
+    if len(starts) <= 1:
+        for s in starts:
+            one(s)
+    else:
+        workers = min(len(starts), os.cpu_count() or 1, 32)
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(one, starts))
     return out
 
 

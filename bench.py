@@ -1,0 +1,601 @@
+#!/usr/bin/env python3
+"""Benchmark of the pipelined GEMM library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload f32_4096|f32_1024|f32_256|f32_ragged|bf16_8192]
+                    [--fill tma|cpasync|sync] [--stages S] [--tile 64|128]
+
+One step is one GEMM of the chosen workload through the library's C ABI with
+inputs resident in device memory; the default is the FP32 GEMM at
+M = N = K = 4096 (seeded uniform[-1,1) operands) through the TMA-ring
+pipelined fill.  L2 is flushed (a 256 MiB device write) before every timed
+step; each step's kernel is timed with CUDA events on the launching stream.
+
+Beside the headline the JSON line carries: the sync / cp.async / TMA fills and
+the stage sweep at the same size (TFLOP/s and t_sync / t_fill), the BF16
+tensor-core GEMM at 8192^3, an end-to-end number through the public API with
+host buffers, the ALU or tensor roofline of the dominant kernel, live clock
+samples, and the CPU oracle timed on the host cores on a bounded sample.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: the GEMM has no exchange step); timing is the max over
+ranks and the value sums the ranks' work.
+
+--impl reference times the CPU oracle itself (plain C, float64, all host
+cores) on the same workload, each step a bounded sample of output rows.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of FP32-FFMA / BF16-tensor peak, pipelined vs sync fill"
+UNIT = "TFLOP/s"
+FP32_FMA_PER_SM_PER_CLK = 128        # FP32 lanes per SM on sm_100-family parts
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0   # GB300 dense BF16, without 2:4 sparsity
+FALLBACK_SM_MAX_MHZ = 2070.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FLUSH_BYTES = 256 << 20              # > 2x the 126 MiB L2
+DEFAULT_LEG = {"f32": dict(fill="tma", stages=4, tile=128), "bf16": dict(fill="tma", stages=4, tile=0)}
+
+
+# --------------------------------------------------------------------- dist
+class Dist:
+    """Rank bookkeeping; torch.distributed only when WORLD_SIZE > 1."""
+
+    def __init__(self, backend: str | None = None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        self.device = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend or "nccl")
+            self.pg = dist
+            self.device = torch.device("cuda", self.local_rank) if (backend or "nccl") == "nccl" else None
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def _reduce(self, x: float, op) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.pg.all_reduce(t, op=op)
+        return float(t.item())
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, None if self.pg is None else self.pg.ReduceOp.MAX)
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, None if self.pg is None else self.pg.ReduceOp.SUM)
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+class CudaTimer:
+    """Per-step CUDA events on the current stream; read after a sync."""
+
+    def __init__(self):
+        import torch
+        self.torch = torch
+        self.pairs = []
+
+    def begin(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.pairs.append([e, None])
+
+    def end(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.pairs[-1][1] = e
+
+    def durations_ms(self):
+        return [a.elapsed_time(b) for a, b in self.pairs]
+
+
+class WallTimer:
+    def __init__(self, sync=lambda: None):
+        self.sync = sync
+        self.t = []
+
+    def begin(self):
+        self.sync()
+        self.t.append([time.perf_counter(), None])
+
+    def end(self):
+        self.sync()
+        self.t[-1][1] = time.perf_counter()
+
+    def durations_ms(self):
+        return [(b - a) * 1e3 for a, b in self.t]
+
+
+def timed_loop(dist: Dist, steps: int, warmup: int, step, flush, timer, sync):
+    """W untimed steps, then exactly K timed steps bracketed by a barrier and a
+    sync on both sides.  Returns (max-over-ranks total ms, local per-step ms)."""
+    for _ in range(warmup):
+        flush()
+        step()
+    sync()
+    dist.barrier()
+    sync()
+    for _ in range(steps):
+        flush()
+        timer.begin()
+        step()
+        timer.end()
+    sync()
+    dist.barrier()
+    sync()
+    per = timer.durations_ms()
+    return dist.max(sum(per)), per
+
+
+# --------------------------------------------------------------------- peaks
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    return {"_source": "fallback", "sm_max_mhz": FALLBACK_SM_MAX_MHZ, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def fp32_peak_tflops(num_sms: int, mhz: float) -> float:
+    return num_sms * FP32_FMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 11:
+                continue
+            try:
+                rows.append(dict(sm=float(f[2]), smax=float(f[3]), power=float(f[4]) if f[4] not in ("[N/A]", "") else 0.0,
+                                 util=float(f[5]) if f[5] not in ("[N/A]", "") else 0.0,
+                                 hw=f[7], hwt=f[8], swt=f[9], swp=f[10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded),
+                "power_w_max": max(r["power"] for r in loaded)}
+
+
+# --------------------------------------------------------------------- profiles
+def kernel_sources_sha() -> str:
+    """Hash of the CUDA sources; a traffic figure captured for other sources is stale."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "async_copy_pipelined_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was captured
+    from the current kernel sources.  Lines read: `source_sha: <hash>` and
+    `traffic_bytes_per_launch[<kernel_key>]: <bytes>`."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    sha, traffic = None, None
+    with open(path) as f:
+        for line in f:
+            line = line.strip().strip("`").strip("- ")
+            if line.startswith("source_sha:"):
+                sha = line.split(":", 1)[1].strip()
+            if line.startswith(f"traffic_bytes_per_launch[{kernel_key}]:"):
+                try:
+                    traffic = float(line.split(":", 1)[1].strip())
+                except ValueError:
+                    traffic = None
+    if sha is None or sha != kernel_sources_sha():
+        return None
+    return traffic
+
+
+# --------------------------------------------------------------------- workloads
+def load_workload(name: str):
+    from async_copy_pipelined_gb300 import inputs
+    w = dict(inputs.WORKLOADS[name])
+    A, B = inputs.workload_operands(name)
+    return w, A, B
+
+
+def to_device(x, cols, dev):
+    import numpy as np
+    import torch
+    if x.dtype == np.uint16:
+        t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(x)
+    return t.to(dev)[:, :cols]
+
+
+def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile):
+    if name.startswith("bf16"):
+        return lambda: pg.gemm_bf16(Ad, Bd, Cd, stages=stages)
+    return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile)
+
+
+def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
+    """Mean / min ms of `launches` calls, each after an L2 flush, events on the stream."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        call()
+    timer = CudaTimer()
+    for _ in range(launches):
+        flush()
+        timer.begin()
+        call()
+        timer.end()
+    torch.cuda.synchronize()
+    d = timer.durations_ms()
+    return statistics.mean(d), min(d)
+
+
+# --------------------------------------------------------------------- oracle leg
+def oracle_sample(name: str, A, B, w, seconds: float, gpu_rows=None):
+    """Time the CPU oracle (float64 definition) on a bounded row sample."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    M, N, K = w["M"], w["N"], w["K"]
+    fn = oracle.gemm_bf16_f64 if name.startswith("bf16") else oracle.gemm_f64
+    cores = oracle.num_threads()
+    probe = max(1, min(M, cores))
+    t0 = time.perf_counter()
+    fn(np.ascontiguousarray(A[:probe]), B, probe, N, K)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(probe, min(M, probe * seconds / max(t_probe, 1e-6))))
+    rows = max(cores, (rows // cores) * cores) if rows >= cores else rows
+    rows = min(rows, M)
+    t0 = time.perf_counter()
+    out = fn(np.ascontiguousarray(A[:rows]), B, rows, N, K)
+    t = time.perf_counter() - t0
+    res = {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"first {rows} of {M} output rows (all {N} columns, K={K}); {t:.2f} s on the host cores",
+           "seconds": t, "rows": rows}
+    if gpu_rows is not None:
+        g = gpu_rows[:rows].astype(np.float64)
+        res["max_abs_diff_vs_gpu"] = float(np.max(np.abs(g - out)))
+    return res
+
+
+def run_reference(args, dist: Dist):
+    """--impl reference: the oracle itself, timed on the host cores."""
+    if dist.rank != 0:
+        return 0
+    name = args.workload
+    w, A, B = load_workload(name)
+    import numpy as np
+    import oracle
+    oracle.build()
+    M, N, K = w["M"], w["N"], w["K"]
+    fn = oracle.gemm_bf16_f64 if name.startswith("bf16") else oracle.gemm_f64
+    cores = oracle.num_threads()
+    t0 = time.perf_counter()
+    fn(np.ascontiguousarray(A[:cores]), B, cores, N, K)
+    per_row = (time.perf_counter() - t0) / cores
+    budget = args.ref_seconds / max(args.steps + args.warmup, 1)
+    rows = int(min(M, max(cores, budget / max(per_row, 1e-9))))
+    Asub = np.ascontiguousarray(A[:rows])
+    for _ in range(args.warmup):
+        fn(Asub, B, rows, N, K)
+    durs = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn(Asub, B, rows, N, K)
+        durs.append(time.perf_counter() - t0)
+    total = sum(durs)
+    value = 2.0 * rows * N * K * args.steps / total / 1e12
+    sample = f"first {rows} of {M} output rows per step (all {N} columns, K={K})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if not name.startswith("bf16") else "f64 (bf16 inputs)", "data": "synthetic",
+        "config": workload_config(name, w, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(name, w, leg):
+    desc = {
+        "f32_256": "fp32 GEMM M=N=K=256, uniform[-1,1) seed 0",
+        "f32_1024": "fp32 GEMM M=N=K=1024, uniform[-1,1) seed 1",
+        "f32_4096": "fp32 GEMM M=N=K=4096, uniform[-1,1) seed 2",
+        "f32_ragged": "fp32 GEMM M=3000 N=5000 K=1000 lda=1003, normal(0,1) seed 3",
+        "bf16_8192": "bf16 GEMM (fp32 accumulate/output) M=N=K=8192, normal(0,0.5)->bf16 seed 4",
+    }[name]
+    cfg = {"workload": desc, "M": w["M"], "N": w["N"], "K": w["K"], "lda": w["lda"],
+           "l2": "flushed before every timed step (256 MiB device write)"}
+    if leg:
+        cfg.update(leg)
+    return cfg
+
+
+# --------------------------------------------------------------------- main leg
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+    import async_copy_pipelined_gb300 as pg
+
+    pg.build()
+    pg.lib()
+    dev = torch.device("cuda", dist.local_rank if dist.world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or FALLBACK_SM_MAX_MHZ)
+    fp32_peak = fp32_peak_tflops(num_sms, sm_max)
+    bf16_peak = float(peaks.get("bf16_tflops") or FALLBACK_BF16_TFLOPS)
+
+    name = args.workload
+    is_bf16 = name.startswith("bf16")
+    leg = dict(DEFAULT_LEG["bf16" if is_bf16 else "f32"])
+    if args.fill:
+        leg["fill"] = args.fill
+    if args.stages is not None:
+        leg["stages"] = args.stages
+    if args.tile is not None:
+        leg["tile"] = args.tile
+    if leg["fill"] == "sync":
+        leg["stages"] = 1
+    w, A, B = load_workload(name)
+    M, N, K = w["M"], w["N"], w["K"]
+    if leg["fill"] == "tma" and not is_bf16 and w["lda"] % 4:
+        # TMA cannot describe a row pitch that is not a multiple of 16 bytes;
+        # the same logical matrix is repacked at the next legal pitch.
+        from async_copy_pipelined_gb300 import inputs
+        A = inputs.workload_operands(name, lda=(w["lda"] + 3) // 4 * 4)[0]
+    flops = 2.0 * M * N * K
+    Ad, Bd = to_device(A, K, dev), to_device(B, N, dev)
+    Cd = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = lambda: flush_buf.zero_()  # noqa: E731
+    call = gemm_call(pg, name, Ad, Bd, Cd, leg["fill"], leg["stages"], leg["tile"])
+
+    # Correctness gate before any timing (the lesson program's rule): the
+    # pipelined result must be bit-identical to the register-path fill.
+    call()
+    gate = {"checked": False}
+    if not is_bf16:
+        Cs = torch.empty_like(Cd)
+        pg.gemm_f32(Ad, Bd, Cs, fill="sync", block_tile=leg["tile"])
+        torch.cuda.synchronize()
+        gate = {"checked": True, "bit_identical_to_sync_fill": bool(torch.equal(Cd.view(torch.int32),
+                                                                                Cs.view(torch.int32)))}
+        del Cs
+        if not gate["bit_identical_to_sync_fill"]:
+            print(json.dumps({"error": "pipelined fill differs from the sync fill", "config": leg}), flush=True)
+            return 1
+    st, detail = pg.device_status()
+    if st != 0:
+        print(json.dumps({"error": f"device status {st} ({detail:#x})"}), flush=True)
+        return 1
+
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid else None)
+    sampler.start()
+    time.sleep(0.3)
+
+    timer = CudaTimer()
+    total_ms, per = timed_loop(dist, args.steps, args.warmup, call, flush, timer, torch.cuda.synchronize)
+    launches = args.steps
+    ms_step = total_ms / args.steps
+    value = dist.world * flops * args.steps / (total_ms / 1e3) / 1e12
+    local_mean = statistics.mean(per)
+    achieved = flops / (local_mean / 1e3) / 1e12
+
+    extras = {}
+    if not args.no_extras and dist.rank == 0:
+        if not is_bf16:
+            fills = {}
+            variants = [("sync", 1, 128), ("sync", 1, 64)]
+            variants += [(f, s, 128) for f in ("cpasync", "tma") for s in (2, 3, 4, 6)]
+            variants += [("cpasync", 2, 64), ("tma", 2, 64)]
+            if w["lda"] % 4:
+                variants = [v for v in variants if v[0] != "tma"]
+            for f, s, t in variants:
+                c = gemm_call(pg, name, Ad, Bd, Cd, f, s, t)
+                mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                launches += args.sweep_launches
+                fills[f"{f}/S{s}/T{t}"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
+                                           "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
+            t_sync = fills["sync/S1/T128"]["ms"]
+            for v in fills.values():
+                v["t_sync_over_t"] = t_sync / v["ms"]
+            extras["fills"] = fills
+            # BF16 tensor-core leg at its own full size.
+            wb, Ab, Bb = load_workload("bf16_8192")
+            Abd, Bbd = to_device(Ab, wb["K"], dev), to_device(Bb, wb["N"], dev)
+            Cbd = torch.empty((wb["M"], wb["N"]), dtype=torch.float32, device=dev)
+            fb = 2.0 * wb["M"] * wb["N"] * wb["K"]
+            cb = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", 4, 0)
+            mean, best = time_kernel(pg, cb, flush, args.sweep_launches)
+            launches += args.sweep_launches
+            tf = fb / (mean / 1e3) / 1e12
+            extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "stages": 4,
+                                   "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak,
+                                                "unit": UNIT, "frac": tf / bf16_peak,
+                                                "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"},
+                                   "frac_nominal_dense_2250": tf / NOMINAL_BF16_DENSE_TFLOPS}
+            del Abd, Bbd, Cbd
+    sampler.stop()
+    clocks = sampler.summary()
+
+    # End to end through the public API with host buffers: pinned H2D of A
+    # and B, the GEMM, D2H of C, every step.
+    e2e = None
+    if dist.rank == 0 or dist.world > 1:
+        Ah = torch.from_numpy(A if not is_bf16 else A.view(np.int16))
+        Bh = torch.from_numpy(B if not is_bf16 else B.view(np.int16))
+        if is_bf16:
+            Ah, Bh = Ah.view(torch.bfloat16), Bh.view(torch.bfloat16)
+        Ah = Ah.pin_memory()[:, :K]
+        Bh = Bh.pin_memory()
+        Ch = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        if is_bf16:
+            host_call = lambda: pg.gemm_bf16(Ah, Bh, Ch, stages=leg["stages"])  # noqa: E731
+        else:
+            host_call = lambda: pg.gemm_f32(Ah, Bh, Ch, fill=leg["fill"], stages=leg["stages"],  # noqa: E731
+                                            block_tile=leg["tile"])
+        e_steps = max(3, min(args.steps, 20))
+        wt = WallTimer()
+        e_total, _ = timed_loop(_NoDist(), e_steps, 3, host_call, lambda: None, wt, torch.cuda.synchronize)
+        e2e = {"value": flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(Ah.element_size() * M * K + Bh.element_size() * K * N),
+               "d2h_bytes_per_step": int(4 * M * N), "ms_per_step": e_total / e_steps}
+        launches_e2e = e_steps
+
+    kernel_key = f"{name}:{leg['fill']}/S{leg['stages']}/T{leg['tile']}"
+    if is_bf16:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": UNIT,
+                "frac": achieved / bf16_peak, "traffic": profiled_traffic(kernel_key),
+                "peak_source": f"{peaks['_source']} (MEASURED_PEAKS bf16_tflops, cuBLAS burst)"}
+    else:
+        roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": UNIT,
+                "frac": achieved / fp32_peak, "traffic": profiled_traffic(kernel_key),
+                "peak_source": f"{num_sms} SMs x {FP32_FMA_PER_SM_PER_CLK} FP32 FMA/clk x 2 x {sm_max:.0f} MHz "
+                               f"({peaks['_source']} max SM clock)"}
+        if clocks.get("sm_mhz"):
+            roof["frac_at_observed_clock"] = achieved / fp32_peak_tflops(num_sms, clocks["sm_mhz"])
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        gpu_rows = Cd[: min(M, 4096)].cpu().numpy()
+        cpu = oracle_sample(name, A, B, w, args.cpu_seconds, gpu_rows=gpu_rows)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, f32 accumulate" if is_bf16 else "f32",
+        "data": "synthetic (seeded SplitMix64 operands, see async_copy_pipelined_gb300/inputs.py)",
+        "config": workload_config(name, w, {**leg, "gate": gate,
+                                            "parallelism": "replicas" if dist.world > 1 else "single GPU"}),
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": launches, "gpu_launches_breakdown": {"timed_steps": args.steps,
+                                                             "sweep_and_bf16_legs": launches - args.steps,
+                                                             "e2e_steps": launches_e2e if e2e else 0},
+        "kernel_sources_sha": kernel_sources_sha(),
+    }
+    line.update(extras)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+class _NoDist(Dist):
+    def __init__(self):
+        self.world, self.rank, self.local_rank, self.pg, self.device = 1, 0, 0, None, None
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="f32_4096",
+                    choices=["f32_256", "f32_1024", "f32_4096", "f32_ragged", "bf16_8192"])
+    ap.add_argument("--fill", choices=["sync", "cpasync", "tma"], default=None)
+    ap.add_argument("--stages", type=int, default=None)
+    ap.add_argument("--tile", type=int, default=None)
+    ap.add_argument("--sweep-launches", type=int, default=20)
+    ap.add_argument("--no-extras", action="store_true", help="time only the main leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0, help="total oracle time budget for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if world > 1 and rank != 0:
+            return 0
+        return run_reference(args, _NoDist())
+    dist = Dist()
+    try:
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+/*
+ * pipelined_gemm.h -- C ABI of the GB300 (sm_103a) pipelined GEMM library.
+ *
+ * The operation is the register-tiled GEMM of "Day 74: Async copies and
+ * pipelines" (section "Two kernels, one arithmetic") and its program
+ * "pipelined_gemm.cu": C = A * B, where the block's shared-memory tiles are
+ * filled one 16-deep K slice at a time and the fill is the only thing that
+ * differs between variants.  Three fills are offered:
+ *
+ *   GEMM_FILL_SYNC     register path: global -> register -> shared, then a
+ *                      CTA barrier ("pipelined_gemm.cu", matmulTileSync;
+ *                      day 74, "A copy that skips the registers").
+ *   GEMM_FILL_CPASYNC  cp.async global -> shared with commit_group /
+ *                      wait_group completion ("A study on CUDA async
+ *                      memcpy", section "async-group based approach";
+ *                      day 74, "Two kernels, one arithmetic").
+ *   GEMM_FILL_TMA      one producer warp issues TMA bulk-tensor copies into
+ *                      a ring of stages guarded by full/empty mbarriers
+ *                      ("A study on CUDA async memcpy", sections "mbarrier
+ *                      based approach" and "block-scoped pipeline"; the
+ *                      producer/consumer split of its "Real world example").
+ *
+ * Every FP32 fill runs the same per-thread FMA micro-kernel, so for every C
+ * element the result is one float32 fused multiply-add chain over k
+ * ascending, starting from +0: the three fills are bit-identical to each
+ * other (the pages' memcmp invariant) and to that chain.
+ *
+ * Layout: all matrices row-major.  A is M x K with leading dimension lda
+ * (element (i,k) at A[i*lda + k]), B is K x N with ldb, C is M x N with ldc.
+ * Elements beyond the logical extents (ragged tiles) are read as zero
+ * ("cp.async", section "Predication is different from zero fill": a partial
+ * source size copies a prefix and zero-fills the rest); padding columns
+ * between K and lda are never read.
+ *
+ * Ownership: every pointer is a device pointer owned by the caller; the
+ * library keeps no reference after the call returns.  The entry points
+ * allocate no memory.
+ *
+ * Asynchrony: gemm_f32 / gemm_bf16 enqueue one kernel on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream) and return without
+ * synchronising.  C is valid once the stream has reached that point.
+ *
+ * Errors: a status code is returned; nothing is enqueued unless the status
+ * is GEMM_OK.  The library never exits the process and never falls back
+ * silently from one fill to another.  A kernel whose internal wait exceeds
+ * its time limit records GEMM_ERR_TIMEOUT in a device status word, which
+ * gemm_device_status() reads.
+ */
+#ifndef PIPELINED_GEMM_H
+#define PIPELINED_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gemm_fill_mode {
+    GEMM_FILL_SYNC = 0,
+    GEMM_FILL_CPASYNC = 1,
+    GEMM_FILL_TMA = 2
+};
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* bad size, leading dimension, pointer, fill, stages or tile   */
+    GEMM_ERR_MISALIGNED = 2,  /* TMA needs 16-byte aligned bases and row pitches              */
+    GEMM_ERR_UNSUPPORTED = 3, /* valid request this build does not implement                  */
+    GEMM_ERR_ARCH = 4,        /* current device is not compute capability 10.3 (sm_103a)      */
+    GEMM_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed (launch, attribute, ...)   */
+    GEMM_ERR_TIMEOUT = 6      /* a kernel's bounded wait expired (read via gemm_device_status) */
+} gemm_status;
+
+/* What a call would launch.  Filled by gemm_f32_plan / gemm_bf16_plan. */
+typedef struct gemm_plan {
+    int fill_mode;       /* GEMM_FILL_*                                                */
+    int block_m;         /* CTA tile rows                                              */
+    int block_n;         /* CTA tile columns                                           */
+    int block_k;         /* K slice depth per pipeline stage                           */
+    int thread_m;        /* micro-tile rows per thread (FP32); 0 for the tensor path   */
+    int thread_n;        /* micro-tile columns per thread (FP32); 0 for tensor path    */
+    int threads;         /* threads per CTA, including any producer / MMA warps        */
+    int stages;          /* shared-memory stages in the ring (1 for the sync fill)     */
+    int a_copy_bytes;    /* bytes per copy instruction for A: 16 (float4 / cp.async.cg),
+                            4 (scalar / cp.async.ca, used when A rows are not 16-byte
+                            aligned), or the TMA box size in bytes                    */
+    int b_copy_bytes;    /* same for B                                                 */
+    int smem_bytes;      /* dynamic shared memory per CTA                              */
+    int grid_x;          /* CTAs launched along x                                      */
+    int grid_y;          /* CTAs launched along y                                      */
+    int k_slices;        /* ceil(K / block_k)                                          */
+} gemm_plan;
+
+/*
+ * gemm_f32: C[M x N] = A[M x K] * B[K x N], float32 in and out.
+ *
+ *   M, N, K     logical sizes, >= 0.  M == 0 or N == 0 is a no-op; K == 0
+ *               writes zeros to C (an empty sum).
+ *   A, lda      device pointer, leading dimension >= max(K, 1).
+ *   B, ldb      device pointer, leading dimension >= max(N, 1).
+ *   C, ldc      device pointer, leading dimension >= max(N, 1).  Only the
+ *               M x N logical elements are written; columns N..ldc-1 are
+ *               left untouched.
+ *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC or GEMM_FILL_TMA.
+ *   stages      sync: 0 or 1.  cp.async / TMA: 2..6, or 0 for the default
+ *               (see gemm_f32_plan).  Each stage is one more slice in flight
+ *               and one more copy of both tiles in shared memory (day 74,
+ *               "Exercise").
+ *   block_tile  64 (64x64 tile, 4x4 micro-tile per thread, 256 threads: the
+ *               lesson's shape), 128 (128x128 tile, 8x8 micro-tile, 256
+ *               threads), or 0 to let the library choose by problem size.
+ *   stream      cudaStream_t to enqueue on.
+ *
+ * Alignment: the sync and cp.async fills accept any lda/ldb; rows that are
+ * not 16-byte aligned are copied with 4-byte operations (reported by
+ * gemm_f32_plan).  The TMA fill requires A and B 16-byte aligned and
+ * lda, ldb multiples of 4 (row pitch a multiple of 16 bytes); otherwise it
+ * returns GEMM_ERR_MISALIGNED.
+ *
+ * Returns GEMM_OK or an error code (nothing enqueued on error).
+ */
+int gemm_f32(int M, int N, int K,
+             const float *A, int lda,
+             const float *B, int ldb,
+             float *C, int ldc,
+             int fill_mode, int stages, int block_tile,
+             void *stream);
+
+/* gemm_f32_plan: validate exactly as gemm_f32 does and describe the launch it
+ * would make, without touching the device.  `plan` is a host pointer. */
+int gemm_f32_plan(int M, int N, int K,
+                  const float *A, int lda,
+                  const float *B, int ldb,
+                  float *C, int ldc,
+                  int fill_mode, int stages, int block_tile,
+                  gemm_plan *plan);
+
+/*
+ * gemm_bf16: C[M x N] (float32) = A[M x K] * B[K x N] with bfloat16 operands
+ * given as raw uint16 bit patterns, products and sums on the 5th-generation
+ * tensor cores (tcgen05.mma, float32 accumulation in tensor memory).  This
+ * is the tensor-core form of the same pipelined GEMM ("异步拷贝与现代
+ * Pipeline", section 6.1 "BF16 GEMM 的异步拷贝": prefetch the next K tile
+ * while the tensor cores work on the current one).
+ *
+ *   fill_mode   GEMM_FILL_TMA (others return GEMM_ERR_UNSUPPORTED).
+ *   stages      2..6, or 0 for the default of 4.
+ *   Alignment   A, B 16-byte aligned; lda, ldb multiples of 8 (16-byte row
+ *               pitch), else GEMM_ERR_MISALIGNED.
+ *   Accuracy    the tensor core's internal summation order is its own, so
+ *               results are not bit-identical to a sequential sum; they
+ *               match the exact-product sum within float32 rounding.
+ * Other arguments, sizes and ownership as gemm_f32.
+ */
+int gemm_bf16(int M, int N, int K,
+              const uint16_t *A, int lda,
+              const uint16_t *B, int ldb,
+              float *C, int ldc,
+              int fill_mode, int stages,
+              void *stream);
+
+int gemm_bf16_plan(int M, int N, int K,
+                   const uint16_t *A, int lda,
+                   const uint16_t *B, int ldb,
+                   float *C, int ldc,
+                   int fill_mode, int stages,
+                   gemm_plan *plan);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *gemm_status_string(int status);
+
+/*
+ * gemm_device_status: synchronise `stream`, then read and clear the current
+ * device's status word.  Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel gave up
+ * on a wait and returned early; its C output is undefined), or
+ * GEMM_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
+ * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
+ * (1 FP32 TMA, 2 BF16, 3 self-test), bits 8-15 the waiting role.
+ */
+int gemm_device_status(void *stream, unsigned int *detail);
+
+/*
+ * gemm_selftest_bounded_wait: launch one CTA whose thread waits on an
+ * mbarrier that nothing ever arrives on, with the same bounded-wait routine
+ * the GEMM kernels use and a limit of `timeout_us` microseconds (1..1000000).
+ * The kernel records GEMM_ERR_TIMEOUT in the status word and returns; read it
+ * with gemm_device_status.  Exists so tests can exercise the timeout path
+ * without ever hanging or faulting the GPU.
+ */
+int gemm_selftest_bounded_wait(int timeout_us, void *stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIPELINED_GEMM_H */

@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+public header declares, and validates / plans requests on the host exactly as
+documented (no compute call is made)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import async_copy_pipelined_gb300 as pg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pg.build()
+    return pg.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "while", "for", "return", "sizeof"):
+                names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("gemm_f32", "gemm_bf16", "gemm_f32_plan", "gemm_bf16_plan", "gemm_status_string",
+              "gemm_device_status", "gemm_selftest_bounded_wait", "gemm_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = pg.library_path()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = _declared_functions() - exported
+    assert not missing, f"declared but not exported: {sorted(missing)}"
+    for n in _declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_build_targets_sm103a_only():
+    """One -gencode, sm_103a: no other architecture, no PTX for JIT."""
+    from async_copy_pipelined_gb300 import buildlib
+    flags = " ".join(buildlib.NVCC_FLAGS)
+    assert flags.count("-gencode") == 1
+    assert "arch=compute_103a,code=sm_103a" in flags
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gemm_version() >= 10000
+    for code in range(7):
+        s = pg.status_string(code)
+        assert s.startswith("GEMM_")
+    assert "unknown" in pg.status_string(99)
+
+
+def _plan(M, N, K, lda=None, ldb=None, ldc=None, fill=2, stages=0, tile=0, a=256, b=256, c=256):
+    p = pg.GemmPlan()
+    st = pg.lib().gemm_f32_plan(M, N, K, a, lda if lda is not None else max(K, 1), b,
+                                ldb if ldb is not None else max(N, 1), c, ldc if ldc is not None else max(N, 1),
+                                fill, stages, tile, ctypes.byref(p))
+    return st, p.as_dict()
+
+
+def test_plan_defaults_and_shapes(lib):
+    st, p = _plan(4096, 4096, 4096, fill=2)
+    assert st == 0 and p["block_m"] == 128 and p["stages"] == 4 and p["threads"] == 288
+    assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (32, 32, 256)
+    st, p = _plan(1024, 1024, 1024, fill=1)
+    assert st == 0 and p["block_m"] == 64 and p["threads"] == 256 and p["stages"] == 3
+    assert (p["grid_x"], p["grid_y"]) == (16, 16)
+    st, p = _plan(256, 256, 256, fill=0)
+    assert st == 0 and p["stages"] == 1 and p["smem_bytes"] == 8192
+    st, p = _plan(3000, 5000, 1000, lda=1003, fill=1, tile=64)
+    assert st == 0 and (p["grid_x"], p["grid_y"]) == (79, 47)
+    assert p["a_copy_bytes"] == 4 and p["b_copy_bytes"] == 16 and p["k_slices"] == 63
+    st, p = _plan(3000, 5000, 1000, lda=1003, fill=1, tile=128)
+    assert st == 0 and (p["grid_x"], p["grid_y"]) == (40, 24)
+    # The lesson's shared-memory arithmetic: one 64x64x16 stage is 8 KiB.
+    for s in (2, 3, 4, 5, 6):
+        st, p = _plan(512, 512, 512, fill=1, stages=s, tile=64)
+        assert st == 0 and p["smem_bytes"] == s * 8192
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1, N=4, K=4), 1),
+    (dict(M=4, N=4, K=4, lda=3), 1),
+    (dict(M=4, N=4, K=4, ldb=3), 1),
+    (dict(M=4, N=4, K=4, ldc=3), 1),
+    (dict(M=4, N=4, K=4, fill=3), 1),
+    (dict(M=4, N=4, K=4, fill=0, stages=2), 1),
+    (dict(M=4, N=4, K=4, fill=1, stages=1), 1),
+    (dict(M=4, N=4, K=4, fill=2, stages=7), 1),
+    (dict(M=4, N=4, K=4, tile=32), 1),
+    (dict(M=4, N=4, K=4, a=0), 1),
+    (dict(M=4, N=4, K=4, c=0), 1),
+    (dict(M=4, N=4, K=4, a=258), 2),
+    (dict(M=4, N=4, K=5, lda=5, fill=2), 2),
+    (dict(M=4, N=4, K=4, a=260, fill=2), 2),
+    (dict(M=65535 * 128 + 1, N=4, K=4, tile=128), 1),
+])
+def test_plan_refusals(lib, kw, code):
+    args = dict(M=4, N=4, K=4)
+    args.update(kw)
+    st, _ = _plan(**args)
+    assert st == code
+
+
+def test_plan_accepts_what_only_some_fills_accept(lib):
+    # lda not a multiple of 4: fine for sync / cp.async (4-byte copies), refused by TMA.
+    assert _plan(4, 4, 5, lda=5, fill=0)[0] == 0
+    assert _plan(4, 4, 5, lda=5, fill=1)[0] == 0
+    assert _plan(4, 4, 5, lda=5, fill=2)[0] == 2
+    # Empty problems are valid; K == 0 allows null A / B.
+    assert _plan(0, 4, 4)[0] == 0
+    assert _plan(4, 4, 0, a=0, b=0)[0] == 0
+
+
+def test_bf16_plan(lib):
+    p = pg.GemmPlan()
+    L = pg.lib()
+    st = L.gemm_bf16_plan(8192, 8192, 8192, 256, 8192, 256, 8192, 256, 8192, 2, 0, ctypes.byref(p))
+    assert st == 0
+    d = p.as_dict()
+    assert (d["block_m"], d["block_n"], d["block_k"], d["stages"]) == (128, 256, 64, 4)
+    assert d["smem_bytes"] <= 227 * 1024 and d["k_slices"] == 128
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 0, ctypes.byref(p)) == 3
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 1, 0, ctypes.byref(p)) == 3
+    assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
+    assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, ctypes.byref(p)) == 1
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    """No silent fallback: with the library path pointing nowhere, the binding raises."""
+    import importlib
+    mod = importlib.import_module("async_copy_pipelined_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mod.lib()

@@ -1,0 +1,115 @@
+"""GPU parity of the BF16 tensor-core path against the oracle, through the C ABI.
+
+The tensor core sums in its own order, so results are compared with the
+exact-product float64 oracle within a tolerance: the benchmark spec's bound
+||C - C_ref||_F / ||C_ref||_F <= 2e-2, and the much tighter per-element bound
+|C - C_ref| <= K * 2^-22 * sum_k |a_ik b_kj| that float32 accumulation of
+exact products satisfies.  Small-integer inputs and the identity / all-ones
+closed forms are exact in any order and are compared bit for bit.
+"""
+import numpy as np
+import pytest
+
+from async_copy_pipelined_gb300 import inputs
+from gpu_util import oracle_bf16_rows, run_bf16, sample_rows
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _abs_products(A, B, M, N, K):
+    Aa = np.abs(inputs.bf16_bits_to_f32(A[:, :K])).astype(np.float64)
+    Ba = np.abs(inputs.bf16_bits_to_f32(B[:, :N])).astype(np.float64)
+    return Aa @ Ba
+
+
+def _check(got, want, absprod, K, what):
+    fro = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300)
+    assert fro <= 2e-2, f"{what}: relative Frobenius error {fro}"
+    bound = K * 2.0 ** -22 * absprod
+    excess = np.abs(got - want) - bound
+    assert np.all(excess <= 0), f"{what}: per-element bound exceeded by {excess.max()}"
+
+
+SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 128), (130, 300, 70), (64, 512, 200), (257, 513, 129),
+          (300, 257, 1000), (1, 700, 64), (700, 1, 64)]
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_ragged_normal(stages, M, N, K):
+    A = inputs.matrix_bf16("normal", M, K, 60 + K, inputs.TAG_A, sigma=0.5)
+    B = inputs.matrix_bf16("normal", K, N, 60 + K, inputs.TAG_B, sigma=0.5)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages)
+    want = oracle.gemm_bf16_f64(A, B, M, N, K)
+    _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 S{stages} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 500), (513, 257, 1000)])
+def test_smallint_exact(M, N, K):
+    A = inputs.matrix_bf16("smallint", M, K, 8, inputs.TAG_A)
+    B = inputs.matrix_bf16("smallint", K, N, 8, inputs.TAG_B)
+    got, _ = run_bf16(A, B, M, N, K)
+    Ai = inputs.bf16_bits_to_f32(A).astype(np.int64)
+    Bi = inputs.bf16_bits_to_f32(B).astype(np.int64)
+    np.testing.assert_array_equal(got, (Ai @ Bi).astype(np.float32))
+
+
+def test_closed_forms():
+    M = N = K = 256
+    B = inputs.matrix_bf16("normal", K, N, 3, inputs.TAG_B, sigma=0.5)
+    ident = inputs.matrix_bf16("identity", M, K, 0, 0)
+    got, _ = run_bf16(ident, B, M, N, K)
+    np.testing.assert_array_equal(got, inputs.bf16_bits_to_f32(B))
+    A = inputs.matrix_bf16("normal", M, K, 3, inputs.TAG_A, sigma=0.5)
+    got, _ = run_bf16(A, inputs.matrix_bf16("identity", K, N, 0, 0), M, N, K)
+    np.testing.assert_array_equal(got, inputs.bf16_bits_to_f32(A))
+    ones_a = inputs.matrix_bf16("ones", M, K, 0, 0)
+    ones_b = inputs.matrix_bf16("ones", K, N, 0, 0)
+    got, _ = run_bf16(ones_a, ones_b, M, N, K)
+    assert np.all(got == np.float32(K))
+
+
+def test_padded_and_ldc_canary():
+    M, N, K = 200, 300, 96
+    A = inputs.matrix_bf16("normal", M, K, 5, inputs.TAG_A, ld=K + 8, sigma=0.5)
+    B = inputs.matrix_bf16("normal", K, N, 5, inputs.TAG_B, ld=N + 16, sigma=0.5)
+    got, full = run_bf16(A, B, M, N, K, ldc=N + 3, sentinel=-5.0)
+    want = oracle.gemm_bf16_f64(A, B, M, N, K)
+    _check(got, want, _abs_products(A, B, M, N, K), K, "padded")
+    assert np.all(full[:, N:] == -5.0)
+
+
+def test_empty_and_k_zero():
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    C = torch.full((3, 9), 4.0, device="cuda")
+    pg.gemm_bf16(torch.empty((3, 0), dtype=torch.bfloat16, device="cuda"),
+                 torch.empty((0, 9), dtype=torch.bfloat16, device="cuda"), C)
+    assert torch.count_nonzero(C).item() == 0
+    C = pg.gemm_bf16(torch.empty((0, 16), dtype=torch.bfloat16, device="cuda"),
+                     torch.ones((16, 8), dtype=torch.bfloat16, device="cuda"))
+    assert C.shape == (0, 8)
+    assert pg.device_status()[0] == 0
+
+
+def test_workload_8192_sampled():
+    """The bf16 workload at full size in the bench's launch configuration,
+    checked on sampled rows (every column) against the exact-product oracle."""
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    w = inputs.WORKLOADS["bf16_8192"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.workload_operands("bf16_8192")
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    Bd = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).cuda()
+    C = pg.gemm_bf16(Ad, Bd)
+    assert pg.device_status()[0] == 0
+    rows = sample_rows(M, 12, seed=4, tiles=(128,))
+    got = C.cpu().numpy()[rows]
+    want = oracle_bf16_rows(A, B, rows, N, K)
+    _check(got, want, _abs_products(np.ascontiguousarray(A[rows]), B, len(rows), N, K), K, "8192^3 sampled")
+    # Repeat: the persistent schedule must give the same bits every run.
+    C2 = pg.gemm_bf16(Ad, Bd)
+    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
