@@ -124,8 +124,8 @@ def _matrix_args(x, name):
     if x.shape[1] > 1 and x.stride(1) != 1:
         raise ValueError(f"{name} must have unit column stride (row-major rows)")
     rows, cols = x.shape
-    ld = x.stride(0) if rows > 1 else max(cols, 1)
-    return rows, cols, max(ld, cols, 1), x.data_ptr()
+    ld = x.stride(0) if x.stride(0) >= cols else cols
+    return rows, cols, max(ld, 1), x.data_ptr()
 
 
 def _check(status: int, what: str):

@@ -99,7 +99,34 @@ def assert_bitwise_equal(got: np.ndarray, want: np.ndarray, what: str):
                              f"got {got[i, j]!r} want {want[i, j]!r}")
 
 
-def f32_operands(kind: str, M: int, N: int, K: int, seed: int, lda: int | None = None, ldb: int | None = None):
+def tma_pitch(n: int) -> int:
+    """Smallest leading dimension >= n whose row pitch is a multiple of 16 bytes
+    (what a TMA tensor map needs for float32 rows)."""
+    return max(4, (n + 3) // 4 * 4)
+
+
+def f32_operands(kind: str, M: int, N: int, K: int, seed: int, lda: int | None = None, ldb: int | None = None,
+                 fill: str | None = None):
+    """Seeded A (M x K) and B (K x N).  For the TMA fill the leading dimensions
+    are raised to the nearest 16-byte row pitch (the same logical values; the
+    extra columns are NaN padding)."""
+    if fill == "tma":
+        lda = tma_pitch(lda or K)
+        ldb = tma_pitch(ldb or N)
     A = inputs.matrix_f32(kind, M, K, seed, inputs.TAG_A, ld=lda)
     B = inputs.matrix_f32(kind, K, N, seed, inputs.TAG_B, ld=ldb)
+    return A, B
+
+
+def bf16_pitch(n: int) -> int:
+    """Smallest leading dimension >= n whose row pitch is a multiple of 16 bytes
+    for bfloat16 rows."""
+    return max(8, (n + 7) // 8 * 8)
+
+
+def bf16_operands(kind: str, M: int, N: int, K: int, seed: int, sigma: float = 0.5,
+                  lda: int | None = None, ldb: int | None = None):
+    """Seeded bfloat16 A (M x K) and B (K x N) at 16-byte row pitches."""
+    A = inputs.matrix_bf16(kind, M, K, seed, inputs.TAG_A, ld=bf16_pitch(lda or K), sigma=sigma)
+    B = inputs.matrix_bf16(kind, K, N, seed, inputs.TAG_B, ld=bf16_pitch(ldb or N), sigma=sigma)
     return A, B

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from async_copy_pipelined_gb300 import inputs
-from gpu_util import oracle_bf16_rows, run_bf16, sample_rows
+from gpu_util import bf16_operands, oracle_bf16_rows, run_bf16, sample_rows
 
 import oracle
 
@@ -39,8 +39,7 @@ SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 128), (130, 300, 70), (64, 512, 
 @pytest.mark.parametrize("stages", [2, 3, 4])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_small_ragged_normal(stages, M, N, K):
-    A = inputs.matrix_bf16("normal", M, K, 60 + K, inputs.TAG_A, sigma=0.5)
-    B = inputs.matrix_bf16("normal", K, N, 60 + K, inputs.TAG_B, sigma=0.5)
+    A, B = bf16_operands("normal", M, N, K, 60 + K)
     got, _ = run_bf16(A, B, M, N, K, stages=stages)
     want = oracle.gemm_bf16_f64(A, B, M, N, K)
     _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 S{stages} {M}x{N}x{K}")
@@ -48,11 +47,10 @@ def test_small_ragged_normal(stages, M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 500), (513, 257, 1000)])
 def test_smallint_exact(M, N, K):
-    A = inputs.matrix_bf16("smallint", M, K, 8, inputs.TAG_A)
-    B = inputs.matrix_bf16("smallint", K, N, 8, inputs.TAG_B)
+    A, B = bf16_operands("smallint", M, N, K, 8)
     got, _ = run_bf16(A, B, M, N, K)
-    Ai = inputs.bf16_bits_to_f32(A).astype(np.int64)
-    Bi = inputs.bf16_bits_to_f32(B).astype(np.int64)
+    Ai = inputs.bf16_bits_to_f32(A[:, :K]).astype(np.int64)
+    Bi = inputs.bf16_bits_to_f32(B[:, :N]).astype(np.int64)
     np.testing.assert_array_equal(got, (Ai @ Bi).astype(np.float32))
 
 
@@ -73,8 +71,7 @@ def test_closed_forms():
 
 def test_padded_and_ldc_canary():
     M, N, K = 200, 300, 96
-    A = inputs.matrix_bf16("normal", M, K, 5, inputs.TAG_A, ld=K + 8, sigma=0.5)
-    B = inputs.matrix_bf16("normal", K, N, 5, inputs.TAG_B, ld=N + 16, sigma=0.5)
+    A, B = bf16_operands("normal", M, N, K, 5, lda=K + 8, ldb=N + 16)
     got, full = run_bf16(A, B, M, N, K, ldc=N + 3, sentinel=-5.0)
     want = oracle.gemm_bf16_f64(A, B, M, N, K)
     _check(got, want, _abs_products(A, B, M, N, K), K, "padded")
