@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/pipelined_gemm.h"
+#include "pipelined_gemm.h"
 
 namespace pg {
 
