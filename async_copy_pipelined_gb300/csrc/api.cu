@@ -119,8 +119,7 @@ int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uin
 // ------------------------------------------------------------ sizes
 int f32_threads(int tile, int fill)
 {
-    (void)tile;
-    return 256 + (fill == GEMM_FILL_TMA ? 32 : 0);
+    return (tile == 32 ? 32 : 256) + (fill == GEMM_FILL_TMA ? 32 : 0);
 }
 
 int f32_smem_bytes(int tile, int fill, int stages)
@@ -172,7 +171,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     if (tile == 0) {
         const long long t128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
         tile = t128 >= kLargeTileMinTiles ? 128 : 64;
-    } else if (tile != 64 && tile != 128) {
+    } else if (tile != 32 && tile != 64 && tile != 128) {
         return GEMM_ERR_INVALID_ARG;
     }
     const bool a_vec = aligned16(A) && (lda % 4) == 0;
@@ -182,7 +181,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         return GEMM_ERR_MISALIGNED;
     const long long grid_y = (M + tile - 1) / tile;
     const long long grid_x = (N + tile - 1) / tile;
-    if (grid_y > 65535 || grid_x > 0x7fffffffLL)
+    if (grid_y > 65535 || grid_x * grid_y > 0x7fffffffLL)
         return GEMM_ERR_INVALID_ARG;
 
     if (plan) {
@@ -191,7 +190,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         plan->block_m = tile;
         plan->block_n = tile;
         plan->block_k = 16;
-        plan->thread_m = tile == 128 ? 8 : 4;
+        plan->thread_m = tile == 64 ? 4 : 8;
         plan->thread_n = tile == 128 ? 8 : 4;
         plan->threads = f32_threads(tile, fill);
         plan->stages = stages;

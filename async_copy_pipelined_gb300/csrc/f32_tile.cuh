@@ -30,10 +30,11 @@ namespace pg {
 template <int BM_, int BN_, int TM_, int TN_, int MIN_BLOCKS_, int MIN_BLOCKS_TMA_>
 struct F32Tile {
     static constexpr int BM = BM_, BN = BN_, BK = 16, TM = TM_, TN = TN_;
-    // Resident CTAs per SM the register budget is sized for.  The TMA fill's
-    // extra producer warp makes 9 warps per CTA; two such CTAs would put 5
-    // warps on one SM sub-partition and cap the 8x8 micro-tile at 96
-    // registers, so the 128-tile TMA kernel runs one CTA per SM instead.
+    // Resident CTAs per SM the register budget is sized for.  The 8x8
+    // micro-tile with double-buffered fragments needs about 140 registers, so
+    // the 128-tile kernels run one CTA (8 consumer warps) per SM; a second
+    // CTA, or the TMA fill's producer warp in two CTAs, would not fit an SM
+    // sub-partition's 16K registers.
     static constexpr int kMinBlocks = MIN_BLOCKS_;
     static constexpr int kMinBlocksTma = MIN_BLOCKS_TMA_;
     static constexpr int kThreadCols = BN / TN;
@@ -56,43 +57,126 @@ struct F32Tile {
                   "each thread moves whole chunks of both slices");
 };
 
-using TileS = F32Tile<64, 64, 4, 4, 4, 4>;   // the lesson's 64x64x16, 4x4, 256 threads
-using TileL = F32Tile<128, 128, 8, 8, 2, 1>; // 128x128x16, 8x8, 256 threads
+// One warp, 32x32 tile, 8x4 micro-tile: the latency-bound shape of "A study
+// on CUDA async memcpy", section "Real world example" (M = N = 32, long K,
+// one block of one warp), where the fill rather than the FMAs sets the pace.
+using TileXS = F32Tile<32, 32, 8, 4, 8, 8>;
+using TileS = F32Tile<64, 64, 4, 4, 4, 3>;   // the lesson's 64x64x16, 4x4, 256 threads
+using TileL = F32Tile<128, 128, 8, 8, 1, 1>; // 128x128x16, 8x8, 256 threads
+
+// CTA -> tile.  CTAs are dispatched in linear order (x fastest); walking
+// kGroupM tile rows down before stepping one tile column right keeps the
+// tiles in flight on a few A row-blocks and B column-blocks at a time, so
+// they are fetched from HBM about once and re-read from L2.  Only the
+// assignment of tiles to CTAs changes, never a value.
+constexpr int kGroupM = 16;
+
+__device__ __forceinline__ void tile_origin(int bm, int bn, int &m0, int &n0)
+{
+    const int tiles_n = static_cast<int>(gridDim.x);
+    const int tiles_m = static_cast<int>(gridDim.y);
+    const int id = static_cast<int>(blockIdx.y) * tiles_n + static_cast<int>(blockIdx.x);
+    const int per_group = kGroupM * tiles_n;
+    const int group = id / per_group;
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, tiles_m - first_m);
+    const int r = id - group * per_group;
+    m0 = (first_m + r % gm) * bm;
+    n0 = (r / gm) * bn;
+}
+
+// One thread's micro-tile of C, held as pairs of adjacent columns: pair p of
+// row i is columns (2p, 2p+1) of the thread's TN columns, packed in one
+// 64-bit register pair so a single fma.rn.f32x2 updates both.
+template <class T>
+struct Accum {
+    unsigned long long pair[T::TM][T::TN / 2];
+
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+            for (int p = 0; p < T::TN / 2; ++p)
+                pair[i][p] = 0ull; // both halves +0.0f
+    }
+};
+
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + d on both halves.  Each half is an independent, correctly
+// rounded fma.rn.f32: the paired form halves the issue slots an FMA costs and
+// changes no result bit.
+__device__ __forceinline__ void fma_f32x2(unsigned long long &d, unsigned long long a, unsigned long long b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// A fragment: rows tr + i*(BM/TM), four consecutive k (one 16-byte load each).
+template <class T>
+__device__ __forceinline__ void load_a_frag(const float *__restrict__ sA, int tr, int kq, float4 (&a)[T::TM])
+{
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i)
+        a[i] = *reinterpret_cast<const float4 *>(sA + (tr + i * T::kThreadRows) * T::BK + kq * 4);
+}
+
+// B fragment of row k: the thread's TN columns as TN/2 column pairs.
+template <class T>
+__device__ __forceinline__ void load_b_frag(const float *__restrict__ sB, int tc, int k,
+                                            unsigned long long (&b)[T::TN / 2])
+{
+#pragma unroll
+    for (int g = 0; g < T::kColGroups; ++g) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(sB + k * T::BN + g * T::kColGroupStride + tc * 4);
+        b[2 * g + 0] = v.x;
+        b[2 * g + 1] = v.y;
+    }
+}
 
 // The inner product all fills share ("pipelined_gemm.cu", computeTile):
 // for each k of the slice, ascending, acc[i][j] = fma(a[i][k], b[k][j],
-// acc[i][j]).  A is read as float4 along k (4 k-steps per load), B as float4
-// along n.  Each C element sees exactly one fused multiply-add per k, in
-// ascending k, whichever fill staged the slice.
+// acc[i][j]).  Each C element sees exactly one fused multiply-add per k, in
+// ascending k, whichever fill staged the slice, so every fill gives the same
+// bits.
+//
+// Register double buffering: the B fragment of k+1 and the A fragment of the
+// next four k are loaded while the FMAs of k run, so shared-memory latency
+// hides behind 32 paired FMAs per k.
 template <class T>
 __device__ __forceinline__ void compute_tile(const float *__restrict__ sA, const float *__restrict__ sB, int tr,
-                                             int tc, float (&acc)[T::TM][T::TN])
+                                             int tc, Accum<T> &acc)
 {
+    float4 a[2][T::TM];
+    unsigned long long b[2][T::TN / 2];
+    load_a_frag<T>(sA, tr, 0, a[0]);
+    load_b_frag<T>(sB, tc, 0, b[0]);
 #pragma unroll
-    for (int kq = 0; kq < T::BK / 4; ++kq) {
-        float4 a4[T::TM];
+    for (int k = 0; k < T::BK; ++k) {
+        const int ab = (k / 4) & 1;
+        const int bb = k & 1;
+        if ((k & 3) == 0 && k + 4 < T::BK)
+            load_a_frag<T>(sA, tr, k / 4 + 1, a[ab ^ 1]);
+        if (k + 1 < T::BK)
+            load_b_frag<T>(sB, tc, k + 1, b[bb ^ 1]);
 #pragma unroll
-        for (int i = 0; i < T::TM; ++i)
-            a4[i] = *reinterpret_cast<const float4 *>(sA + (tr + i * T::kThreadRows) * T::BK + kq * 4);
+        for (int i = 0; i < T::TM; ++i) {
+            const int kk = k & 3;
+            const float av = kk == 0 ? a[ab][i].x : kk == 1 ? a[ab][i].y : kk == 2 ? a[ab][i].z : a[ab][i].w;
+            const unsigned long long aa = pack_f32x2(av, av);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            float b[T::TN];
-#pragma unroll
-            for (int g = 0; g < T::kColGroups; ++g) {
-                const float4 v =
-                    *reinterpret_cast<const float4 *>(sB + (kq * 4 + kk) * T::BN + g * T::kColGroupStride + tc * 4);
-                b[4 * g + 0] = v.x;
-                b[4 * g + 1] = v.y;
-                b[4 * g + 2] = v.z;
-                b[4 * g + 3] = v.w;
-            }
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i) {
-                const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
-#pragma unroll
-                for (int j = 0; j < T::TN; ++j)
-                    acc[i][j] = __fmaf_rn(a, b[j], acc[i][j]);
-            }
+            for (int p = 0; p < T::TN / 2; ++p)
+                fma_f32x2(acc.pair[i][p], aa, b[bb][p]);
         }
     }
 }
@@ -168,8 +252,7 @@ __device__ __forceinline__ void b_chunk_coords(int c, int k0, int n0, int &k, in
 
 // Write the micro-tile; rows >= M and columns >= N are skipped.
 template <class T>
-__device__ __forceinline__ void store_tile(const F32Args &p, int m0, int n0, int tr, int tc,
-                                           const float (&acc)[T::TM][T::TN])
+__device__ __forceinline__ void store_tile(const F32Args &p, int m0, int n0, int tr, int tc, const Accum<T> &acc)
 {
 #pragma unroll
     for (int i = 0; i < T::TM; ++i) {
@@ -180,27 +263,19 @@ __device__ __forceinline__ void store_tile(const F32Args &p, int m0, int n0, int
 #pragma unroll
         for (int g = 0; g < T::kColGroups; ++g) {
             const int col = n0 + g * T::kColGroupStride + tc * 4;
+            float v[4];
+            unpack_f32x2(acc.pair[i][2 * g], v[0], v[1]);
+            unpack_f32x2(acc.pair[i][2 * g + 1], v[2], v[3]);
             if (p.c_vec && col + 4 <= p.N) {
-                *reinterpret_cast<float4 *>(crow + col) =
-                    make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2], acc[i][4 * g + 3]);
+                *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (col + e < p.N)
-                        crow[col + e] = acc[i][4 * g + e];
+                        crow[col + e] = v[e];
             }
         }
     }
-}
-
-template <class T>
-__device__ __forceinline__ void zero_acc(float (&acc)[T::TM][T::TN])
-{
-#pragma unroll
-    for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < T::TN; ++j)
-            acc[i][j] = 0.0f;
 }
 
 } // namespace pg

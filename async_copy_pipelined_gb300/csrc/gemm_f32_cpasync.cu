@@ -28,8 +28,8 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
     extern __shared__ __align__(1024) float smem[];
 
     const int tid = threadIdx.x;
-    const int m0 = blockIdx.y * T::BM;
-    const int n0 = blockIdx.x * T::BN;
+    int m0, n0;
+    tile_origin(T::BM, T::BN, m0, n0);
     const int tr = tid / T::kThreadCols;
     const int tc = tid % T::kThreadCols;
     const int k_slices = (p.K + T::BK - 1) / T::BK;
@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
         }
     };
 
-    float acc[T::TM][T::TN];
-    zero_acc<T>(acc);
+    Accum<T> acc;
+    acc.zero();
 
     // Prologue: slices 0 .. S-2 in flight, one group each.
 #pragma unroll
@@ -107,6 +107,8 @@ static int launch_cpasync_tile(const F32Args &a, cudaStream_t s)
 
 int launch_f32_cpasync(const F32Args &a, cudaStream_t s)
 {
+    if (a.tile == 32)
+        return launch_cpasync_tile<TileXS>(a, s);
     return a.tile == 128 ? launch_cpasync_tile<TileL>(a, s) : launch_cpasync_tile<TileS>(a, s);
 }
 

@@ -20,13 +20,13 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_sync_kern
     float *sB = smem + T::kAFloats;
 
     const int tid = threadIdx.x;
-    const int m0 = blockIdx.y * T::BM;
-    const int n0 = blockIdx.x * T::BN;
+    int m0, n0;
+    tile_origin(T::BM, T::BN, m0, n0);
     const int tr = tid / T::kThreadCols;
     const int tc = tid % T::kThreadCols;
 
-    float acc[T::TM][T::TN];
-    zero_acc<T>(acc);
+    Accum<T> acc;
+    acc.zero();
 
     const int k_slices = (p.K + T::BK - 1) / T::BK;
     for (int kt = 0; kt < k_slices; ++kt) {
@@ -86,6 +86,8 @@ static int launch_sync_t(const F32Args &a, cudaStream_t s)
 
 int launch_f32_sync(const F32Args &a, cudaStream_t s)
 {
+    if (a.tile == 32)
+        return launch_sync_t<TileXS>(a, s);
     return a.tile == 128 ? launch_sync_t<TileL>(a, s) : launch_sync_t<TileS>(a, s);
 }
 

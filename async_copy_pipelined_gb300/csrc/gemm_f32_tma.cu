@@ -44,8 +44,8 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
     const int tid = threadIdx.x;
     const int warp = tid / 32;
     const int lane = tid % 32;
-    const int m0 = blockIdx.y * T::BM;
-    const int n0 = blockIdx.x * T::BN;
+    int m0, n0;
+    tile_origin(T::BM, T::BN, m0, n0);
     const int k_slices = (p.K + T::BK - 1) / T::BK;
 
     if (tid == 0)
@@ -82,8 +82,8 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
     // -------------------------------------------------------------- consumers
     const int tr = tid / T::kThreadCols;
     const int tc = tid % T::kThreadCols;
-    float acc[T::TM][T::TN];
-    zero_acc<T>(acc);
+    Accum<T> acc;
+    acc.zero();
 
     for (int kt = 0; kt < k_slices; ++kt) {
         const bool ok = ring.consumer_wait(kt, p.wait_limit_ns);
@@ -140,6 +140,8 @@ static int launch_tma_tile(const F32Args &a, cudaStream_t s)
 
 int launch_f32_tma(const F32Args &a, cudaStream_t s)
 {
+    if (a.tile == 32)
+        return launch_tma_tile<TileXS>(a, s);
     return a.tile == 128 ? launch_tma_tile<TileL>(a, s) : launch_tma_tile<TileS>(a, s);
 }
 

@@ -201,6 +201,9 @@ WORKLOADS = {
     "f32_4096": dict(M=4096, N=4096, K=4096, lda=4096, kind="uniform", sigma=1.0, seed=2),
     "f32_ragged": dict(M=3000, N=5000, K=1000, lda=1003, kind="normal", sigma=1.0, seed=3),
     "bf16_8192": dict(M=8192, N=8192, K=8192, lda=8192, kind="normal", sigma=0.5, seed=4),
+    # The latency-bound shape of "A study on CUDA async memcpy" ("Real world
+    # example": M = N = 32, K = 65536, one block); seed 5 is this library's choice.
+    "f32_tallk": dict(M=32, N=32, K=65536, lda=65536, kind="uniform", sigma=1.0, seed=5),
 }
 
 

@@ -375,6 +375,7 @@ def workload_config(name, w, leg):
         "f32_4096": "fp32 GEMM M=N=K=4096, uniform[-1,1) seed 2",
         "f32_ragged": "fp32 GEMM M=3000 N=5000 K=1000 lda=1003, normal(0,1) seed 3",
         "bf16_8192": "bf16 GEMM (fp32 accumulate/output) M=N=K=8192, normal(0,0.5)->bf16 seed 4",
+        "f32_tallk": "fp32 GEMM M=N=32 K=65536 (one CTA), uniform[-1,1) seed 5",
     }[name]
     cfg = {"workload": desc, "M": w["M"], "N": w["N"], "K": w["K"], "lda": w["lda"],
            "l2": "flushed before every timed step (256 MiB device write)"}
@@ -476,6 +477,22 @@ def run_ours(args, dist: Dist):
             for v in fills.values():
                 v["t_sync_over_t"] = t_sync / v["ms"]
             extras["fills"] = fills
+            # The latency-bound tall-K shape on the one-warp 32x32 tile: one
+            # CTA walks 4096 slices, so the fill's latency is the whole story.
+            wt, At, Bt = load_workload("f32_tallk")
+            Atd, Btd = to_device(At, wt["K"], dev), to_device(Bt, wt["N"], dev)
+            Ctd = torch.empty((wt["M"], wt["N"]), dtype=torch.float32, device=dev)
+            ft = 2.0 * wt["M"] * wt["N"] * wt["K"]
+            tall = {}
+            for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("tma", 2), ("tma", 4)):
+                c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
+                mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                launches += args.sweep_launches
+                tall[f"{f}/S{s}/T32"] = {"us": mean * 1e3, "gflops": ft / (mean / 1e3) / 1e9}
+            for v in tall.values():
+                v["t_sync_over_t"] = tall["sync/S1/T32"]["us"] / v["us"]
+            extras["tallk_32x32x65536"] = tall
+            del Atd, Btd, Ctd
             # BF16 tensor-core leg at its own full size.
             wb, Ab, Bb = load_workload("bf16_8192")
             Abd, Bbd = to_device(Ab, wb["K"], dev), to_device(Bb, wb["N"], dev)
@@ -567,7 +584,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="f32_4096",
-                    choices=["f32_256", "f32_1024", "f32_4096", "f32_ragged", "bf16_8192"])
+                    choices=["f32_256", "f32_1024", "f32_4096", "f32_ragged", "f32_tallk", "bf16_8192"])
     ap.add_argument("--fill", choices=["sync", "cpasync", "tma"], default=None)
     ap.add_argument("--stages", type=int, default=None)
     ap.add_argument("--tile", type=int, default=None)

@@ -108,7 +108,10 @@ typedef struct gemm_plan {
  *               "Exercise").
  *   block_tile  64 (64x64 tile, 4x4 micro-tile per thread, 256 threads: the
  *               lesson's shape), 128 (128x128 tile, 8x8 micro-tile, 256
- *               threads), or 0 to let the library choose by problem size.
+ *               threads), 32 (32x32 tile, 8x4 micro-tile, one warp: the
+ *               latency-bound shape of "A study on CUDA async memcpy",
+ *               "Real world example"), or 0 to let the library choose by
+ *               problem size (64 or 128).
  *   stream      cudaStream_t to enqueue on.
  *
  * Alignment: the sync and cp.async fills accept any lda/ldb; rows that are

@@ -86,6 +86,11 @@ def test_plan_defaults_and_shapes(lib):
     assert p["a_copy_bytes"] == 4 and p["b_copy_bytes"] == 16 and p["k_slices"] == 63
     st, p = _plan(3000, 5000, 1000, lda=1003, fill=1, tile=128)
     assert st == 0 and (p["grid_x"], p["grid_y"]) == (40, 24)
+    st, p = _plan(32, 32, 65536, fill=2, tile=32)
+    assert st == 0 and p["threads"] == 64 and (p["thread_m"], p["thread_n"]) == (8, 4)
+    assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (1, 1, 4096)
+    st, p = _plan(32, 32, 65536, fill=1, tile=32)
+    assert st == 0 and p["threads"] == 32 and p["smem_bytes"] == 3 * 4096
     # The lesson's shared-memory arithmetic: one 64x64x16 stage is 8 KiB.
     for s in (2, 3, 4, 5, 6):
         st, p = _plan(512, 512, 512, fill=1, stages=s, tile=64)
@@ -101,7 +106,7 @@ def test_plan_defaults_and_shapes(lib):
     (dict(M=4, N=4, K=4, fill=0, stages=2), 1),
     (dict(M=4, N=4, K=4, fill=1, stages=1), 1),
     (dict(M=4, N=4, K=4, fill=2, stages=7), 1),
-    (dict(M=4, N=4, K=4, tile=32), 1),
+    (dict(M=4, N=4, K=4, tile=16), 1),
     (dict(M=4, N=4, K=4, a=0), 1),
     (dict(M=4, N=4, K=4, c=0), 1),
     (dict(M=4, N=4, K=4, a=258), 2),

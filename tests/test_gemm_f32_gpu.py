@@ -175,6 +175,23 @@ def test_workload_ragged_lda_k_plus_3():
     assert np.max(np.abs(got - oracle_f64_rows(A, B, rows, N, K))) <= 1e-5 * K
 
 
+# ----------------------------------------------------- tall K, one warp
+
+def test_workload_tallk_one_warp_all_fills():
+    """M = N = 32, K = 65536 on the one-warp 32x32 tile: every fill and stage
+    count equals the oracle's FMA chain bit for bit (4096 slices each)."""
+    w = inputs.WORKLOADS["f32_tallk"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.workload_operands("f32_tallk")
+    want32 = oracle.gemm_fmaf_chain(A, B, M, N, K)
+    want64 = oracle.gemm_f64(A, B, M, N, K)
+    for fill, stages in [("sync", 1), ("cpasync", 2), ("cpasync", 4), ("cpasync", 6), ("tma", 2), ("tma", 4),
+                         ("tma", 6)]:
+        got, _ = run_f32(A, B, M, N, K, fill, stages, 32)
+        assert_bitwise_equal(got, want32, f"tall-K {fill}/S{stages}")
+    assert np.max(np.abs(got - want64)) <= 1e-5 * K
+
+
 # ----------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("fill", ["sync", "cpasync", "tma"])
