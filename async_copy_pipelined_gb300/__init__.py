@@ -27,7 +27,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libpipelined_gemm.so")
 
-FILL = {"sync": 0, "cpasync": 1, "tma": 2}
+FILL = {"sync": 0, "cpasync": 1, "tma": 2, "cpasync_mbar": 3}
 
 GEMM_OK = 0
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_UNSUPPORTED",

@@ -129,7 +129,7 @@ int f32_smem_bytes(int tile, int fill, int stages)
         return stage_bytes;
     if (fill == GEMM_FILL_CPASYNC)
         return stages * stage_bytes;
-    return stages * stage_bytes + 16 * stages + 1024; // + barriers + alignment slack
+    return stages * stage_bytes + 16 * stages + 1024; // TMA / mbarrier ring: + barriers + alignment slack
 }
 
 int bf16_threads() { return 192; }
@@ -149,7 +149,8 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
 {
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA)
+    if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA &&
+        fill != GEMM_FILL_CPASYNC_MBAR)
         return GEMM_ERR_INVALID_ARG;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
         return GEMM_ERR_INVALID_ARG;
@@ -232,7 +233,7 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
 {
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_SYNC || fill == GEMM_FILL_CPASYNC)
+    if (fill == GEMM_FILL_SYNC || fill == GEMM_FILL_CPASYNC || fill == GEMM_FILL_CPASYNC_MBAR)
         return GEMM_ERR_UNSUPPORTED;
     if (fill != GEMM_FILL_TMA)
         return GEMM_ERR_INVALID_ARG;
@@ -362,6 +363,7 @@ int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int l
     switch (fill_mode) {
     case GEMM_FILL_SYNC: return launch_f32_sync(args, s);
     case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);
+    case GEMM_FILL_CPASYNC_MBAR: return launch_f32_cpasync_mbar(args, s);
     default: return launch_f32_tma(args, s);
     }
 }

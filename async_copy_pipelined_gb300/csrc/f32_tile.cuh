@@ -61,7 +61,7 @@ struct F32Tile {
 // on CUDA async memcpy", section "Real world example" (M = N = 32, long K,
 // one block of one warp), where the fill rather than the FMAs sets the pace.
 using TileXS = F32Tile<32, 32, 8, 4, 8, 8>;
-using TileS = F32Tile<64, 64, 4, 4, 4, 3>;   // the lesson's 64x64x16, 4x4, 256 threads
+using TileS = F32Tile<64, 64, 4, 4, 2, 2>;   // the lesson's 64x64x16, 4x4, 256 threads
 using TileL = F32Tile<128, 128, 8, 8, 1, 1>; // 128x128x16, 8x8, 256 threads
 
 // CTA -> tile.  CTAs are dispatched in linear order (x fastest); walking
@@ -248,6 +248,31 @@ __device__ __forceinline__ void b_chunk_coords(int c, int k0, int n0, int &k, in
 {
     k = k0 + c / T::kBChunksPerRow;
     n = n0 + (c % T::kBChunksPerRow) * 4;
+}
+
+// Issue this thread's cp.async copies of slice kt into the stage at `stage`
+// (A slice then B slice).  Completion is tracked by the caller: a commit
+// group (cp.async fill) or an mbarrier arrive (mbarrier-completed fill).
+template <class T>
+__device__ __forceinline__ void issue_slice_cpasync(float *stage, const F32Args &p, int tid, int m0, int n0, int kt)
+{
+    float *sA = stage;
+    float *sB = stage + T::kAFloats;
+    const int k0 = kt * T::BK;
+#pragma unroll
+    for (int q = 0; q < T::kAChunksPerThread; ++q) {
+        const int c = tid + q * T::kThreads;
+        int r, k;
+        a_chunk_coords<T>(c, m0, k0, r, k);
+        cp_chunk_guarded(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec);
+    }
+#pragma unroll
+    for (int q = 0; q < T::kBChunksPerThread; ++q) {
+        const int c = tid + q * T::kThreads;
+        int k, n;
+        b_chunk_coords<T>(c, k0, n0, k, n);
+        cp_chunk_guarded(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec);
+    }
 }
 
 // Write the micro-tile; rows >= M and columns >= N are skipped.

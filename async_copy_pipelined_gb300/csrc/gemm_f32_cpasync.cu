@@ -35,23 +35,7 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
     const int k_slices = (p.K + T::BK - 1) / T::BK;
 
     auto issue = [&](int stage, int kt) {
-        float *sA = smem + stage * T::kStageFloats;
-        float *sB = sA + T::kAFloats;
-        const int k0 = kt * T::BK;
-#pragma unroll
-        for (int q = 0; q < T::kAChunksPerThread; ++q) {
-            const int c = tid + q * T::kThreads;
-            int r, k;
-            a_chunk_coords<T>(c, m0, k0, r, k);
-            cp_chunk_guarded(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec);
-        }
-#pragma unroll
-        for (int q = 0; q < T::kBChunksPerThread; ++q) {
-            const int c = tid + q * T::kThreads;
-            int k, n;
-            b_chunk_coords<T>(c, k0, n0, k, n);
-            cp_chunk_guarded(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec);
-        }
+        issue_slice_cpasync<T>(smem + stage * T::kStageFloats, p, tid, m0, n0, kt);
     };
 
     Accum<T> acc;

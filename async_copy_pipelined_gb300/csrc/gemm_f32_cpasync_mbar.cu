@@ -1,0 +1,138 @@
+// FP32 GEMM, fill (d): cp.async whose completion is tracked by mbarriers.
+//
+// The block-scoped pipeline of "A study on CUDA async memcpy" (sections
+// "mbarrier based approach" and "block-scoped pipeline") as it comes out of
+// the lesson's cuda::pipeline ("Day 74: Async copies and pipelines",
+// "Results": the piped kernel lowers to cp.async plus
+// cp.async.mbarrier.arrive).  Every thread is both producer and consumer, as
+// in the lesson, but completion is no longer a per-thread group count plus a
+// CTA barrier:
+//
+//   producer_acquire  wait empty[s]: all 8 warps have released the stage
+//   memcpy_async      this thread's cp.async copies of the slice
+//   producer_commit   cp.async.mbarrier.arrive.noinc full[s]: the barrier's
+//                     phase completes once all 256 threads' copies landed
+//   consumer_wait     wait full[s]
+//   consumer_release  one arrive per warp on empty[s]
+//
+// No CTA-wide barrier sits in the main loop; a warp only waits for the
+// slowest warp of the slice whose stage it is about to refill (one slice of
+// slack).  Zero fill, chunk mapping and the inner product are those of the
+// cp.async fill, so results are bit-identical to the other fills.  Waits are
+// bounded; on expiry the warp records GEMM_ERR_TIMEOUT and stops, and every
+// thread drains its own copies (cp.async.wait_all) before exit.
+#include "f32_tile.cuh"
+#include "tma_ring.cuh"
+
+namespace pg {
+
+template <class T, int S>
+__global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_mbar_kernel(const F32Args p)
+{
+    static_assert(S >= 2 && S <= 6, "stages");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = align_smem(smem_u32(smem_raw), 1024);
+    float *stage0 = reinterpret_cast<float *>(smem_raw + (base - smem_u32(smem_raw)));
+    const uint32_t bars = base + S * T::kStageBytes;
+    const uint32_t full0 = bars;
+    const uint32_t empty0 = bars + 8u * S;
+    constexpr int kWarps = T::kThreads / 32;
+
+    const int tid = threadIdx.x;
+    const int lane = tid % 32;
+    int m0, n0;
+    tile_origin(T::BM, T::BN, m0, n0);
+    const int tr = tid / T::kThreadCols;
+    const int tc = tid % T::kThreadCols;
+    const int k_slices = (p.K + T::BK - 1) / T::BK;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, T::kThreads); // one asynchronous arrival per thread
+            mbar_init(empty0 + 8u * s, kWarps);     // one release per warp
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto full_bar = [&](int f) { return full0 + 8u * static_cast<uint32_t>(f % S); };
+    auto empty_bar = [&](int f) { return empty0 + 8u * static_cast<uint32_t>(f % S); };
+    auto parity = [](int f) { return static_cast<uint32_t>((f / S) & 1); };
+    auto issue = [&](int f) {
+        issue_slice_cpasync<T>(stage0 + (f % S) * T::kStageFloats, p, tid, m0, n0, f);
+        cp_async_mbar_arrive_noinc(full_bar(f));
+    };
+
+    Accum<T> acc;
+    acc.zero();
+    bool ok = true;
+
+    // Prologue: the first S-1 slices go into fresh stages.
+    for (int f = 0; f < S - 1 && f < k_slices; ++f)
+        issue(f);
+
+    for (int kt = 0; kt < k_slices; ++kt) {
+        const int fetch = kt + S - 1;
+        if (fetch < k_slices) {
+            // The stage was last used by slice kt-1: wait until every warp released it.
+            const bool free = mbar_wait_bounded(empty_bar(fetch), parity(fetch) ^ 1u, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, free)) {
+                if (lane == 0)
+                    record_error(p.status, kErrFamilyF32CpAsyncMbar | kErrRoleProducer);
+                ok = false;
+                break;
+            }
+            issue(fetch);
+        }
+        const bool landed = mbar_wait_bounded(full_bar(kt), parity(kt), p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, landed)) {
+            if (lane == 0)
+                record_error(p.status, kErrFamilyF32CpAsyncMbar | kErrRoleConsumer);
+            ok = false;
+            break;
+        }
+        const float *sA = stage0 + (kt % S) * T::kStageFloats;
+        compute_tile<T>(sA, sA + T::kAFloats, tr, tc, acc);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty_bar(kt));
+    }
+    cp_async_wait_all(); // none of this thread's copies may land after it exits
+
+    if (ok)
+        store_tile<T>(p, m0, n0, tr, tc, acc);
+}
+
+template <class T, int S>
+static int launch_cpasync_mbar_t(const F32Args &a, cudaStream_t s)
+{
+    const int smem = f32_smem_bytes(T::BM, GEMM_FILL_CPASYNC_MBAR, S);
+    if (cudaFuncSetAttribute(gemm_f32_cpasync_mbar_kernel<T, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
+    gemm_f32_cpasync_mbar_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+template <class T>
+static int launch_cpasync_mbar_tile(const F32Args &a, cudaStream_t s)
+{
+    switch (a.stages) {
+    case 2: return launch_cpasync_mbar_t<T, 2>(a, s);
+    case 3: return launch_cpasync_mbar_t<T, 3>(a, s);
+    case 4: return launch_cpasync_mbar_t<T, 4>(a, s);
+    case 5: return launch_cpasync_mbar_t<T, 5>(a, s);
+    case 6: return launch_cpasync_mbar_t<T, 6>(a, s);
+    default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s)
+{
+    if (a.tile == 32)
+        return launch_cpasync_mbar_tile<TileXS>(a, s);
+    return a.tile == 128 ? launch_cpasync_mbar_tile<TileL>(a, s) : launch_cpasync_mbar_tile<TileS>(a, s);
+}
+
+} // namespace pg

@@ -45,6 +45,7 @@ struct Bf16Args {
 int launch_f32_sync(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync(const F32Args &a, cudaStream_t s);
 int launch_f32_tma(const F32Args &a, cudaStream_t s);
+int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s);
 int launch_f32_zero(const F32Args &a, cudaStream_t s);
 int launch_bf16_tma(const Bf16Args &a, cudaStream_t s);
 int launch_bf16_zero(const Bf16Args &a, cudaStream_t s);
@@ -68,6 +69,7 @@ int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uin
 constexpr unsigned int kErrFamilyF32Tma = 1;
 constexpr unsigned int kErrFamilyBf16 = 2;
 constexpr unsigned int kErrFamilySelftest = 3;
+constexpr unsigned int kErrFamilyF32CpAsyncMbar = 4;
 constexpr unsigned int kErrRoleConsumer = 1u << 8;
 constexpr unsigned int kErrRoleProducer = 2u << 8;
 constexpr unsigned int kErrRoleMma = 3u << 8;

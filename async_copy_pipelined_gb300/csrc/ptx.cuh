@@ -39,6 +39,19 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
+// Make `bar` track this thread's prior cp.async copies: one arrive-on is
+// triggered on the barrier when they have all completed.  .noinc: the
+// barrier's expected count already includes that arrival.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
 // Wait until at most N of this thread's committed groups are still pending.
 template <int N>
 __device__ __forceinline__ void cp_async_wait()

@@ -463,8 +463,8 @@ def run_ours(args, dist: Dist):
         if not is_bf16:
             fills = {}
             variants = [("sync", 1, 128), ("sync", 1, 64)]
-            variants += [(f, s, 128) for f in ("cpasync", "tma") for s in (2, 3, 4, 6)]
-            variants += [("cpasync", 2, 64), ("tma", 2, 64)]
+            variants += [(f, s, 128) for f in ("cpasync", "tma", "cpasync_mbar") for s in (2, 3, 4, 6)]
+            variants += [("cpasync", 2, 64), ("tma", 2, 64), ("cpasync_mbar", 2, 64)]
             if w["lda"] % 4:
                 variants = [v for v in variants if v[0] != "tma"]
             for f, s, t in variants:
@@ -484,7 +484,8 @@ def run_ours(args, dist: Dist):
             Ctd = torch.empty((wt["M"], wt["N"]), dtype=torch.float32, device=dev)
             ft = 2.0 * wt["M"] * wt["N"] * wt["K"]
             tall = {}
-            for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("tma", 2), ("tma", 4)):
+            for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("tma", 2), ("tma", 4), ("cpasync_mbar", 2),
+                         ("cpasync_mbar", 4)):
                 c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
                 mean, best = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
@@ -585,7 +586,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="f32_4096",
                     choices=["f32_256", "f32_1024", "f32_4096", "f32_ragged", "f32_tallk", "bf16_8192"])
-    ap.add_argument("--fill", choices=["sync", "cpasync", "tma"], default=None)
+    ap.add_argument("--fill", choices=["sync", "cpasync", "tma", "cpasync_mbar"], default=None)
     ap.add_argument("--stages", type=int, default=None)
     ap.add_argument("--tile", type=int, default=None)
     ap.add_argument("--sweep-launches", type=int, default=20)

@@ -19,6 +19,13 @@
  *                      ("A study on CUDA async memcpy", sections "mbarrier
  *                      based approach" and "block-scoped pipeline"; the
  *                      producer/consumer split of its "Real world example").
+ *   GEMM_FILL_CPASYNC_MBAR
+ *                      cp.async whose completion is tracked by a full/empty
+ *                      mbarrier ring (cp.async.mbarrier.arrive.noinc): the
+ *                      form the lesson's block-scoped cuda::pipeline lowers
+ *                      to (day 74, "Results"; "A study on CUDA async
+ *                      memcpy", "block-scoped pipeline").  Every thread
+ *                      copies and computes; no CTA barrier in the loop.
  *
  * Every FP32 fill runs the same per-thread FMA micro-kernel, so for every C
  * element the result is one float32 fused multiply-add chain over k
@@ -58,7 +65,8 @@ extern "C" {
 enum gemm_fill_mode {
     GEMM_FILL_SYNC = 0,
     GEMM_FILL_CPASYNC = 1,
-    GEMM_FILL_TMA = 2
+    GEMM_FILL_TMA = 2,
+    GEMM_FILL_CPASYNC_MBAR = 3
 };
 
 typedef enum gemm_status {
@@ -101,8 +109,9 @@ typedef struct gemm_plan {
  *   C, ldc      device pointer, leading dimension >= max(N, 1).  Only the
  *               M x N logical elements are written; columns N..ldc-1 are
  *               left untouched.
- *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC or GEMM_FILL_TMA.
- *   stages      sync: 0 or 1.  cp.async / TMA: 2..6, or 0 for the default
+ *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA or
+ *               GEMM_FILL_CPASYNC_MBAR.
+ *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default
  *               (see gemm_f32_plan).  Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
  *               "Exercise").
@@ -114,7 +123,7 @@ typedef struct gemm_plan {
  *               problem size (64 or 128).
  *   stream      cudaStream_t to enqueue on.
  *
- * Alignment: the sync and cp.async fills accept any lda/ldb; rows that are
+ * Alignment: the sync and both cp.async fills accept any lda/ldb; rows that are
  * not 16-byte aligned are copied with 4-byte operations (reported by
  * gemm_f32_plan).  The TMA fill requires A and B 16-byte aligned and
  * lda, ldb multiples of 4 (row pitch a multiple of 16 bytes); otherwise it
@@ -146,7 +155,7 @@ int gemm_f32_plan(int M, int N, int K,
  * Pipeline", section 6.1 "BF16 GEMM 的异步拷贝": prefetch the next K tile
  * while the tensor cores work on the current one).
  *
- *   fill_mode   GEMM_FILL_TMA (others return GEMM_ERR_UNSUPPORTED).
+ *   fill_mode   GEMM_FILL_TMA (the other fills return GEMM_ERR_UNSUPPORTED).
  *   stages      2..6, or 0 for the default of 4.
  *   Alignment   A, B 16-byte aligned; lda, ldb multiples of 8 (16-byte row
  *               pitch), else GEMM_ERR_MISALIGNED.
@@ -178,7 +187,8 @@ const char *gemm_status_string(int status);
  * on a wait and returned early; its C output is undefined), or
  * GEMM_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
- * (1 FP32 TMA, 2 BF16, 3 self-test), bits 8-15 the waiting role.
+ * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async),
+ * bits 8-15 the waiting role.
  */
 int gemm_device_status(void *stream, unsigned int *detail);
 

@@ -79,6 +79,9 @@ def test_plan_defaults_and_shapes(lib):
     st, p = _plan(1024, 1024, 1024, fill=1)
     assert st == 0 and p["block_m"] == 64 and p["threads"] == 256 and p["stages"] == 3
     assert (p["grid_x"], p["grid_y"]) == (16, 16)
+    st, p = _plan(4096, 4096, 4096, fill=3, stages=4)
+    assert st == 0 and p["threads"] == 256 and p["a_copy_bytes"] == 16
+    assert p["smem_bytes"] == 4 * 16384 + 16 * 4 + 1024
     st, p = _plan(256, 256, 256, fill=0)
     assert st == 0 and p["stages"] == 1 and p["smem_bytes"] == 8192
     st, p = _plan(3000, 5000, 1000, lda=1003, fill=1, tile=64)
@@ -102,7 +105,7 @@ def test_plan_defaults_and_shapes(lib):
     (dict(M=4, N=4, K=4, lda=3), 1),
     (dict(M=4, N=4, K=4, ldb=3), 1),
     (dict(M=4, N=4, K=4, ldc=3), 1),
-    (dict(M=4, N=4, K=4, fill=3), 1),
+    (dict(M=4, N=4, K=4, fill=4), 1),
     (dict(M=4, N=4, K=4, fill=0, stages=2), 1),
     (dict(M=4, N=4, K=4, fill=1, stages=1), 1),
     (dict(M=4, N=4, K=4, fill=2, stages=7), 1),
@@ -125,6 +128,7 @@ def test_plan_accepts_what_only_some_fills_accept(lib):
     # lda not a multiple of 4: fine for sync / cp.async (4-byte copies), refused by TMA.
     assert _plan(4, 4, 5, lda=5, fill=0)[0] == 0
     assert _plan(4, 4, 5, lda=5, fill=1)[0] == 0
+    assert _plan(4, 4, 5, lda=5, fill=3)[0] == 0
     assert _plan(4, 4, 5, lda=5, fill=2)[0] == 2
     # Empty problems are valid; K == 0 allows null A / B.
     assert _plan(0, 4, 4)[0] == 0
@@ -141,6 +145,7 @@ def test_bf16_plan(lib):
     assert d["smem_bytes"] <= 227 * 1024 and d["k_slices"] == 128
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 0, ctypes.byref(p)) == 3
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 1, 0, ctypes.byref(p)) == 3
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 3, 0, ctypes.byref(p)) == 3
     assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
     assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, ctypes.byref(p)) == 1

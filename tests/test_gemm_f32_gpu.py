@@ -99,7 +99,8 @@ def test_workload_1024_fills_bit_identical():
     want64 = oracle.gemm_f64(A, B, M, N, K)
     outs = {}
     for fill, stages, tile in [("sync", 1, 64), ("cpasync", 2, 64), ("tma", 2, 64), ("sync", 1, 128),
-                               ("cpasync", 4, 128), ("tma", 4, 128)]:
+                               ("cpasync", 4, 128), ("tma", 4, 128), ("cpasync_mbar", 2, 64),
+                               ("cpasync_mbar", 4, 128)]:
         got, _ = run_f32(A, B, M, N, K, fill, stages, tile)
         outs[(fill, stages, tile)] = got
         assert_bitwise_equal(got, want32, f"1024^3 {fill}/S{stages}/T{tile}")
@@ -125,7 +126,8 @@ def test_workload_4096_stage_sweep_sampled():
     Bd = torch.from_numpy(B).cuda()
     ref = pg.gemm_f32(Ad, Bd, fill="sync", block_tile=128)
     for fill, stages in [("cpasync", 2), ("cpasync", 3), ("cpasync", 4), ("cpasync", 6),
-                         ("tma", 2), ("tma", 3), ("tma", 4), ("tma", 6)]:
+                         ("tma", 2), ("tma", 3), ("tma", 4), ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4),
+                         ("cpasync_mbar", 6)]:
         out = pg.gemm_f32(Ad, Bd, fill=fill, stages=stages, block_tile=128)
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"{fill}/S{stages} != sync"
     out64 = pg.gemm_f32(Ad, Bd, fill="tma", stages=4, block_tile=64)
@@ -156,7 +158,7 @@ def test_workload_ragged_lda_k_plus_3():
     assert plan["a_copy_bytes"] == 4 and plan["b_copy_bytes"] == 16
     outs = {}
     for fill, stages, tile in [("sync", 1, 64), ("sync", 1, 128), ("cpasync", 2, 64), ("cpasync", 3, 128),
-                               ("cpasync", 6, 128)]:
+                               ("cpasync", 6, 128), ("cpasync_mbar", 3, 128), ("cpasync_mbar", 2, 64)]:
         outs[(fill, stages, tile)] = pg.gemm_f32(Ad, Bd, fill=fill, stages=stages, block_tile=tile)
     with pytest.raises(pg.GemmError) as e:
         pg.gemm_f32(Ad, Bd, fill="tma", stages=4)
@@ -186,7 +188,7 @@ def test_workload_tallk_one_warp_all_fills():
     want32 = oracle.gemm_fmaf_chain(A, B, M, N, K)
     want64 = oracle.gemm_f64(A, B, M, N, K)
     for fill, stages in [("sync", 1), ("cpasync", 2), ("cpasync", 4), ("cpasync", 6), ("tma", 2), ("tma", 4),
-                         ("tma", 6)]:
+                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4)]:
         got, _ = run_f32(A, B, M, N, K, fill, stages, 32)
         assert_bitwise_equal(got, want32, f"tall-K {fill}/S{stages}")
     assert np.max(np.abs(got - want64)) <= 1e-5 * K
@@ -194,7 +196,7 @@ def test_workload_tallk_one_warp_all_fills():
 
 # ----------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("fill", ["sync", "cpasync", "tma"])
+@pytest.mark.parametrize("fill", ["sync", "cpasync", "tma", "cpasync_mbar"])
 def test_empty_sizes(fill):
     import torch
     import async_copy_pipelined_gb300 as pg
@@ -217,7 +219,8 @@ def test_page4_pattern_all_fills():
     b = inputs.matrix_f32("page4b", n, n, 0, 0)
     want = oracle.gemm_fmaf_chain(a, b, n, n, n)
     want64 = oracle.gemm_f64(a, b, n, n, n)
-    for fill, stages, tile in [("sync", 1, 64), ("cpasync", 2, 64), ("tma", 2, 64), ("tma", 4, 128)]:
+    for fill, stages, tile in [("sync", 1, 64), ("cpasync", 2, 64), ("tma", 2, 64), ("tma", 4, 128),
+                               ("cpasync_mbar", 2, 64)]:
         got, _ = run_f32(a, b, n, n, n, fill, stages, tile)
         assert_bitwise_equal(got, want, f"page-4 pattern {fill}")
         # The program's own relative check (rel 1e-4, scale 1 at zero) holds too.
