@@ -143,10 +143,11 @@ def plan_f32(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_
     return p.as_dict()
 
 
-def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, stages=0, a_ptr=256, b_ptr=256, c_ptr=256) -> dict:
+def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, a_ptr=256, b_ptr=256,
+              c_ptr=256) -> dict:
     p = GemmPlan()
     st = lib().gemm_bf16_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
-                              FILL["tma"], stages, ctypes.byref(p))
+                              _fill_code(fill), stages, ctypes.byref(p))
     _check(st, "gemm_bf16_plan")
     return p.as_dict()
 
@@ -195,11 +196,14 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     return C
 
 
-def gemm_bf16(A, B, C=None, *, stages=0, stream=None):
-    """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores."""
+def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
+    """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores.
+
+    fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
+    the MMAs read; all three give the same bits."""
     import torch
     if not A.is_cuda:
-        return _host_roundtrip(lambda a, b, _c: gemm_bf16(a, b, None, stages=stages, stream=stream),
+        return _host_roundtrip(lambda a, b, _c: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=stream),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")
@@ -212,7 +216,7 @@ def gemm_bf16(A, B, C=None, *, stages=0, stream=None):
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
-    st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, FILL["tma"], stages, _stream_handle(stream))
+    st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, _stream_handle(stream))
     _check(st, "gemm_bf16")
     return C
 

@@ -132,7 +132,6 @@ int f32_smem_bytes(int tile, int fill, int stages)
     return stages * stage_bytes + 16 * stages + 1024; // TMA / mbarrier ring: + barriers + alignment slack
 }
 
-int bf16_threads() { return 192; }
 
 int bf16_smem_bytes(int stages)
 {
@@ -233,19 +232,26 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
 {
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_SYNC || fill == GEMM_FILL_CPASYNC || fill == GEMM_FILL_CPASYNC_MBAR)
+    if (fill == GEMM_FILL_CPASYNC_MBAR)
         return GEMM_ERR_UNSUPPORTED;
-    if (fill != GEMM_FILL_TMA)
+    if (fill != GEMM_FILL_TMA && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_SYNC)
         return GEMM_ERR_INVALID_ARG;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
         return GEMM_ERR_INVALID_ARG;
     const bool work = M > 0 && N > 0;
     if (work && (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))))
         return GEMM_ERR_INVALID_ARG;
-    if (stages == 0)
-        stages = kDefaultStagesBf16;
-    if (stages < 2 || stages > kMaxStagesBf16)
-        return GEMM_ERR_INVALID_ARG;
+    if (fill == GEMM_FILL_SYNC) {
+        // The register-path fill has one stage: loads and MMAs alternate.
+        if (stages != 0 && stages != 1)
+            return GEMM_ERR_INVALID_ARG;
+        stages = 1;
+    } else {
+        if (stages == 0)
+            stages = kDefaultStagesBf16;
+        if (stages < 2 || stages > kMaxStagesBf16)
+            return GEMM_ERR_INVALID_ARG;
+    }
     if (!aligned4(C))
         return GEMM_ERR_MISALIGNED;
     if (work && K > 0 && (!aligned16(A) || !aligned16(B) || (lda % 8) != 0 || (ldb % 8) != 0))
@@ -260,10 +266,10 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         plan->block_m = kBf16BlockM;
         plan->block_n = kBf16BlockN;
         plan->block_k = kBf16BlockK;
-        plan->threads = bf16_threads();
+        plan->threads = bf16_threads(fill);
         plan->stages = stages;
-        plan->a_copy_bytes = kBf16BlockM * kBf16BlockK * 2;
-        plan->b_copy_bytes = kBf16BlockK * 64 * 2;
+        plan->a_copy_bytes = fill == GEMM_FILL_TMA ? kBf16BlockM * kBf16BlockK * 2 : 16;
+        plan->b_copy_bytes = fill == GEMM_FILL_TMA ? kBf16BlockK * 64 * 2 : 16;
         plan->smem_bytes = bf16_smem_bytes(stages);
         plan->grid_x = static_cast<int>(tiles_m * tiles_n); // upper bound; capped at the SM count on launch
         plan->grid_y = 1;
@@ -396,7 +402,7 @@ int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return launch_bf16_zero(args, s);
-    return launch_bf16_tma(args, s);
+    return launch_bf16(args, fill_mode, s);
 }
 
 int gemm_device_status(void *stream, unsigned int *detail)

@@ -1,5 +1,5 @@
-// BF16 -> FP32 GEMM on the 5th-generation tensor cores, fed by the same TMA
-// ring as the FP32 TMA fill.
+// BF16 -> FP32 GEMM on the 5th-generation tensor cores, fed by the same ring
+// of full/empty mbarriers as the FP32 TMA fill, with three ways to fill it.
 //
 // The pages' tensor-core loop ("异步拷贝与现代 Pipeline", section 6.1
 // "BF16 GEMM 的异步拷贝": prefetch the next K tile, commit, compute the current
@@ -19,6 +19,20 @@
 //               hand the accumulator back.  With two accumulators the
 //               epilogue of tile i overlaps the MMAs of tile i+1.
 //
+// The fills, as in the FP32 family ("Day 74: Async copies and pipelines", day
+// 80's goal of this pipeline feeding tensor cores):
+//   TMA       as above: one thread, one descriptor per box.
+//   cp.async  four producer warps copy 16-byte chunks straight into the
+//             swizzled stage with cp.async, keep one stage in flight per
+//             thread (wait_group 1), and mark a stage full once their own
+//             copies of it have landed.
+//   sync      four producer warps load chunks into registers and store them
+//             into the one and only stage; loads and MMAs strictly alternate.
+// The cp.async and sync producers write the 128-byte-swizzled layout the TMA
+// would write (16-byte chunk index XOR row mod 8 within each 1024-byte atom)
+// through the generic proxy; each writer issues fence.proxy.async before its
+// mbarrier arrive so the tensor core (async proxy) sees the data.
+//
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ... in
 // groups of 16 M-tiles so the tiles in flight share A and B rows in L2.
 // Ragged M, N, K: TMA zero-fills out-of-range box elements (zeros add nothing
@@ -30,6 +44,8 @@
 //   B stage  four 64(n) x 64(k) boxes, each 64 rows (k) of 128 bytes (64 n):
 //            N-major ("MN-major"); 64-column atoms 8192 B apart (LBO), 8-row K
 //            groups 1024 B apart (SBO); the K step advances 16 rows = 2048 B.
+#include <cstring>
+
 #include "gemm_internal.h"
 #include "ptx.cuh"
 #include "tma_ring.cuh"
@@ -48,7 +64,18 @@ constexpr uint32_t kBTileBytes = BN * BK * 2;              // 32 KiB
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 KiB
 constexpr uint32_t kTmemCols = 2 * BN;                     // two accumulators
 constexpr int kGroupM = 16;
-constexpr int kThreads = 192;
+constexpr int kStageChunks = kStageBytes / 16;           // 3072 16-byte chunks per stage
+constexpr int kCopyWarps = 4;                             // cp.async / sync producer warps
+constexpr int kCopyThreads = kCopyWarps * 32;
+
+template <int Fill>
+struct Roles {
+    static constexpr int kProducerWarps = Fill == GEMM_FILL_TMA ? 1 : kCopyWarps;
+    static constexpr int kMmaWarp = kProducerWarps;
+    static constexpr int kEpiWarp0 = kMmaWarp + 1;        // four epilogue warps
+    static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+    static constexpr uint32_t kFullArrivals = Fill == GEMM_FILL_TMA ? 1u : static_cast<uint32_t>(kCopyThreads);
+};
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = BF16
 // (bits 7-9 = 1), B = BF16 (bits 10-12 = 1), A K-major (bit 15 = 0), B
@@ -82,12 +109,61 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 }
 } // namespace bf16
 
-template <int S>
-__global__ void __launch_bounds__(bf16::kThreads, 1)
+namespace bf16 {
+// 16-byte chunk q (0 .. 3071) of the stage for tile (mb, nb), K block kb:
+// chunks 0..1023 are the A box (row r = q/8 of 128, chunk c = q%8 of the
+// 128-byte K row), the rest the four B boxes (box j, K row r of 64, chunk c
+// of the 128-byte N row).  Gives the global element (row, col) of the
+// chunk's first value, whether it is an A chunk, and its byte offset in the
+// 128-byte-swizzled stage.
+__device__ __forceinline__ void stage_chunk(int q, int mb, int nb, int kb, int &grow, int &gcol, bool &is_a,
+                                            uint32_t &dst)
+{
+    if (q < BM * 8) {
+        const int r = q >> 3, c = q & 7;
+        is_a = true;
+        grow = mb * BM + r;
+        gcol = kb * BK + c * 8;
+        dst = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+    } else {
+        q -= BM * 8;
+        const int j = q >> 9, r = (q >> 3) & 63, c = q & 7;
+        is_a = false;
+        grow = kb * BK + r;
+        gcol = nb * BN + j * static_cast<int>(kBBoxCols) + c * 8;
+        dst = kATileBytes + static_cast<uint32_t>(j) * kBBoxBytes +
+              static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+    }
+}
+
+// Eight consecutive bfloat16 (row, col..col+7) of an R x C row-major matrix,
+// zero outside it; a full in-range chunk is one 16-byte load.
+__device__ __forceinline__ uint4 load_chunk_bf16(const uint16_t *__restrict__ base, long long ld, int row, int col,
+                                                 int R, int C)
+{
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < R && col < C) {
+        const uint16_t *src = base + static_cast<long long>(row) * ld + col;
+        if (col + 8 <= C) {
+            v = *reinterpret_cast<const uint4 *>(src);
+        } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int e = 0; e < 8 && col + e < C; ++e)
+                w[e >> 1] |= static_cast<uint32_t>(src[e]) << (16 * (e & 1));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    return v;
+}
+} // namespace bf16
+
+template <int Fill, int S>
+__global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const Bf16Args p)
 {
     using namespace bf16;
+    using R = Roles<Fill>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align_smem(raw, 1024);
@@ -108,7 +184,7 @@ __global__ void __launch_bounds__(bf16::kThreads, 1)
     const int k_blocks = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
-        ring.init(1);
+        ring.init(1, R::kFullArrivals);
         mbar_init(tmem_full0, 1);
         mbar_init(tmem_full0 + 8u, 1);
         mbar_init(tmem_empty0, 4);
@@ -117,7 +193,7 @@ __global__ void __launch_bounds__(bf16::kThreads, 1)
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == R::kMmaWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -126,7 +202,7 @@ __global__ void __launch_bounds__(bf16::kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
 
-    if (warp == 0) {
+    if (Fill == GEMM_FILL_TMA && warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             tma_prefetch_map(&map_a);
@@ -159,7 +235,78 @@ __global__ void __launch_bounds__(bf16::kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (Fill != GEMM_FILL_TMA && warp < R::kProducerWarps) {
+        // ------------------------------------------- cp.async / sync producers
+        const int ptid = threadIdx.x;
+        int f = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, tiles_m, tiles_n, mb, nb);
+            for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                const bool free = ring.producer_acquire(f, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, free)) {
+                    if (lane == 0)
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleProducer);
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
+                if constexpr (Fill == GEMM_FILL_CPASYNC) {
+                    for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
+                        int grow, gcol;
+                        bool is_a;
+                        uint32_t off;
+                        stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
+                        const uint16_t *gbase = is_a ? p.A : p.B;
+                        const long long ld = is_a ? p.lda : p.ldb;
+                        const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
+                        uint32_t nbytes = 0;
+                        const uint16_t *src = gbase;
+                        if (grow < rows && gcol < cols) {
+                            nbytes = static_cast<uint32_t>(min(cols - gcol, 8)) * 2u;
+                            src = gbase + static_cast<long long>(grow) * ld + gcol;
+                        }
+                        cp_async_cg16(dst + off, src, nbytes);
+                    }
+                    cp_async_commit();
+                    if (f > 0) {
+                        cp_async_wait<1>(); // this thread's copies of the previous stage have landed
+                        fence_proxy_async_smem();
+                        mbar_arrive(ring.full_bar(f - 1));
+                    }
+                } else {
+                    constexpr int kBatch = 8;
+                    for (int q0 = ptid; q0 < kStageChunks; q0 += kBatch * kCopyThreads) {
+                        uint4 v[kBatch];
+                        uint32_t off[kBatch];
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            int grow, gcol;
+                            bool is_a;
+                            stage_chunk(q0 + b * kCopyThreads, mb, nb, kb, grow, gcol, is_a, off[b]);
+                            v[b] = is_a ? load_chunk_bf16(p.A, p.lda, grow, gcol, p.M, p.K)
+                                        : load_chunk_bf16(p.B, p.ldb, grow, gcol, p.K, p.N);
+                        }
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst + off[b]), "r"(v[b].x),
+                                         "r"(v[b].y), "r"(v[b].z), "r"(v[b].w)
+                                         : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(ring.full_bar(f));
+                }
+            }
+        }
+        if constexpr (Fill == GEMM_FILL_CPASYNC) {
+            cp_async_wait<0>();
+            if (ok && f > 0) {
+                fence_proxy_async_smem();
+                mbar_arrive(ring.full_bar(f - 1));
+            }
+        }
+    } else if (warp == R::kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int f = 0;
@@ -206,7 +353,7 @@ __global__ void __launch_bounds__(bf16::kThreads, 1)
         tc_fence_after_sync();
         __syncwarp();
         tmem_dealloc(tmem_base, kTmemCols);
-    } else {
+    } else if (warp >= R::kEpiWarp0) {
         // ------------------------------------------------------- epilogue
         const int quarter = warp & 3; // tensor-memory lanes 32*quarter .. +31
         const bool c_vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
@@ -269,36 +416,57 @@ __global__ void gemm_bf16_zero_kernel(float *C, int M, int N, long long ldc)
         C[(idx / N) * ldc + idx % N] = 0.0f;
 }
 
-template <int S>
+template <int Fill, int S>
 static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
 {
     using namespace bf16;
     alignas(64) CUtensorMap map_a;
     alignas(64) CUtensorMap map_b;
-    int st = encode_tensor_map_2d(&map_a, 1, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                                  static_cast<uint64_t>(a.lda) * 2u, BK, BM, 1);
-    if (st != GEMM_OK)
-        return st;
-    st = encode_tensor_map_2d(&map_b, 1, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.ldb) * 2u, kBBoxCols, BK, 1);
-    if (st != GEMM_OK)
-        return st;
+    if constexpr (Fill == GEMM_FILL_TMA) {
+        int st = encode_tensor_map_2d(&map_a, 1, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                                      static_cast<uint64_t>(a.lda) * 2u, BK, BM, 1);
+        if (st != GEMM_OK)
+            return st;
+        st = encode_tensor_map_2d(&map_b, 1, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                                  static_cast<uint64_t>(a.ldb) * 2u, kBBoxCols, BK, 1);
+        if (st != GEMM_OK)
+            return st;
+    } else {
+        // The register and cp.async fills read A and B through plain pointers.
+        std::memset(&map_a, 0, sizeof map_a);
+        std::memset(&map_b, 0, sizeof map_b);
+    }
     const int smem = bf16_smem_bytes(S);
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<Fill, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return GEMM_ERR_CUDA;
     const long long tiles = static_cast<long long>((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);
-    gemm_bf16_tc_kernel<S><<<grid, kThreads, smem, s>>>(map_a, map_b, a);
+    gemm_bf16_tc_kernel<Fill, S><<<grid, Roles<Fill>::kThreads, smem, s>>>(map_a, map_b, a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-int launch_bf16_tma(const Bf16Args &a, cudaStream_t s)
+int bf16_threads(int fill)
 {
+    return fill == GEMM_FILL_TMA ? bf16::Roles<GEMM_FILL_TMA>::kThreads : bf16::Roles<GEMM_FILL_CPASYNC>::kThreads;
+}
+
+int launch_bf16(const Bf16Args &a, int fill, cudaStream_t s)
+{
+    if (fill == GEMM_FILL_SYNC)
+        return a.stages == 1 ? launch_bf16_t<GEMM_FILL_SYNC, 1>(a, s) : GEMM_ERR_INVALID_ARG;
+    if (fill == GEMM_FILL_CPASYNC) {
+        switch (a.stages) {
+        case 2: return launch_bf16_t<GEMM_FILL_CPASYNC, 2>(a, s);
+        case 3: return launch_bf16_t<GEMM_FILL_CPASYNC, 3>(a, s);
+        case 4: return launch_bf16_t<GEMM_FILL_CPASYNC, 4>(a, s);
+        default: return GEMM_ERR_INVALID_ARG;
+        }
+    }
     switch (a.stages) {
-    case 2: return launch_bf16_t<2>(a, s);
-    case 3: return launch_bf16_t<3>(a, s);
-    case 4: return launch_bf16_t<4>(a, s);
+    case 2: return launch_bf16_t<GEMM_FILL_TMA, 2>(a, s);
+    case 3: return launch_bf16_t<GEMM_FILL_TMA, 3>(a, s);
+    case 4: return launch_bf16_t<GEMM_FILL_TMA, 4>(a, s);
     default: return GEMM_ERR_INVALID_ARG;
     }
 }

@@ -47,7 +47,7 @@ int launch_f32_cpasync(const F32Args &a, cudaStream_t s);
 int launch_f32_tma(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s);
 int launch_f32_zero(const F32Args &a, cudaStream_t s);
-int launch_bf16_tma(const Bf16Args &a, cudaStream_t s);
+int launch_bf16(const Bf16Args &a, int fill, cudaStream_t s);
 int launch_bf16_zero(const Bf16Args &a, cudaStream_t s);
 int launch_selftest_wait(unsigned int *status, unsigned long long limit_ns, cudaStream_t s);
 
@@ -55,7 +55,7 @@ int launch_selftest_wait(unsigned int *status, unsigned long long limit_ns, cuda
 int f32_smem_bytes(int tile, int fill, int stages);
 int f32_threads(int tile, int fill);
 int bf16_smem_bytes(int stages);
-int bf16_threads();
+int bf16_threads(int fill);
 constexpr int kBf16BlockM = 128;
 constexpr int kBf16BlockN = 256;
 constexpr int kBf16BlockK = 64;

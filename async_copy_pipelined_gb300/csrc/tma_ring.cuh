@@ -29,12 +29,13 @@ struct TmaRing {
     __device__ __forceinline__ static uint32_t parity(int f) { return static_cast<uint32_t>((f / S) & 1); }
 
     // One thread, before the CTA barrier that publishes the ring.
-    // full: one arrival (the producer's arrive.expect_tx) plus the TMA bytes.
-    // empty: `releases` arrivals per consumption.
-    __device__ __forceinline__ void init(uint32_t releases) const
+    // full: `fills` arrivals per filling (1: the TMA producer's
+    // arrive.expect_tx, completed by the copy bytes; or one per copying
+    // thread).  empty: `releases` arrivals per consumption.
+    __device__ __forceinline__ void init(uint32_t releases, uint32_t fills = 1) const
     {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8u * s, 1);
+            mbar_init(full0 + 8u * s, fills);
             mbar_init(empty0 + 8u * s, releases);
         }
         fence_barrier_init();

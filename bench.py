@@ -278,7 +278,7 @@ def to_device(x, cols, dev):
 
 def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile):
     if name.startswith("bf16"):
-        return lambda: pg.gemm_bf16(Ad, Bd, Cd, stages=stages)
+        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages)
     return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile)
 
 
@@ -508,6 +508,15 @@ def run_ours(args, dist: Dist):
                                                 "unit": UNIT, "frac": tf / bf16_peak,
                                                 "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"},
                                    "frac_nominal_dense_2250": tf / NOMINAL_BF16_DENSE_TFLOPS}
+            bfills = {}
+            for f, s in (("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 4), ("sync", 1)):
+                c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, f, s, 0)
+                m2, b2 = time_kernel(pg, c, flush, args.sweep_launches)
+                launches += args.sweep_launches
+                bfills[f"{f}/S{s}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2}
+            for v in bfills.values():
+                v["t_sync_over_t"] = bfills["sync/S1"]["ms"] / v["ms"]
+            extras["bf16_8192"]["fills"] = bfills
             del Abd, Bbd, Cbd
     sampler.stop()
     clocks = sampler.summary()

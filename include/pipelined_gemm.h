@@ -155,8 +155,14 @@ int gemm_f32_plan(int M, int N, int K,
  * Pipeline", section 6.1 "BF16 GEMM 的异步拷贝": prefetch the next K tile
  * while the tensor cores work on the current one).
  *
- *   fill_mode   GEMM_FILL_TMA (the other fills return GEMM_ERR_UNSUPPORTED).
- *   stages      2..6, or 0 for the default of 4.
+ *   fill_mode   GEMM_FILL_TMA (one thread issues 2-D tensor copies),
+ *               GEMM_FILL_CPASYNC (four producer warps copy 16-byte chunks
+ *               with cp.async into the same swizzled stages), or
+ *               GEMM_FILL_SYNC (the register path: producers load and
+ *               store, one stage, loads and MMAs alternate).
+ *               GEMM_FILL_CPASYNC_MBAR returns GEMM_ERR_UNSUPPORTED.
+ *   stages      TMA / cp.async: 2..4 (4 x 48 KiB fills shared memory), or
+ *               0 for the default of 4.  sync: 0 or 1.
  *   Alignment   A, B 16-byte aligned; lda, ldb multiples of 8 (16-byte row
  *               pitch), else GEMM_ERR_MISALIGNED.
  *   Accuracy    the tensor core's internal summation order is its own, so

@@ -57,12 +57,14 @@ def test_refusals_enqueue_nothing():
     # The same view is fine for the sync / cp.async fills (4-byte copies).
     out = pg.gemm_f32(buf[:, 1:65], B, fill="cpasync")
     assert torch.all(out == 64.0)
-    # bf16 with a register or cp.async fill is not implemented.
+    # bf16 with the mbarrier-completed cp.async fill is not implemented; the
+    # register-path fill has exactly one stage.
     Ab = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
     lib = pg.lib()
-    for fill in (0, 1):
-        st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, fill, 0, None)
-        assert st == 3
+    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 3, 0, None)
+    assert st == 3
+    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 0, 2, None)
+    assert st == 1
     st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 2, 6, None)
     assert st == 1  # stages above what fits in shared memory
     torch.cuda.synchronize()

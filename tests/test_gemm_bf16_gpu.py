@@ -36,19 +36,27 @@ SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 128), (130, 300, 70), (64, 512, 
           (300, 257, 1000), (1, 700, 64), (700, 1, 64)]
 
 
-@pytest.mark.parametrize("stages", [2, 3, 4])
+BF16_FILLS = [("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 3), ("cpasync", 4), ("sync", 1)]
+
+
+@pytest.mark.parametrize("fill,stages", BF16_FILLS)
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_small_ragged_normal(stages, M, N, K):
+def test_small_ragged_normal(fill, stages, M, N, K):
     A, B = bf16_operands("normal", M, N, K, 60 + K)
-    got, _ = run_bf16(A, B, M, N, K, stages=stages)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
     want = oracle.gemm_bf16_f64(A, B, M, N, K)
-    _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 S{stages} {M}x{N}x{K}")
+    _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} {M}x{N}x{K}")
+    # Every fill feeds the same MMA sequence with the same bytes: same bits.
+    if fill != "tma":
+        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma")
+        np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("fill,stages", [("tma", 4), ("cpasync", 3), ("sync", 1)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 500), (513, 257, 1000)])
-def test_smallint_exact(M, N, K):
+def test_smallint_exact(fill, stages, M, N, K):
     A, B = bf16_operands("smallint", M, N, K, 8)
-    got, _ = run_bf16(A, B, M, N, K)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
     Ai = inputs.bf16_bits_to_f32(A[:, :K]).astype(np.int64)
     Bi = inputs.bf16_bits_to_f32(B[:, :N]).astype(np.int64)
     np.testing.assert_array_equal(got, (Ai @ Bi).astype(np.float32))
@@ -107,6 +115,11 @@ def test_workload_8192_sampled():
     got = C.cpu().numpy()[rows]
     want = oracle_bf16_rows(A, B, rows, N, K)
     _check(got, want, _abs_products(np.ascontiguousarray(A[rows]), B, len(rows), N, K), K, "8192^3 sampled")
-    # Repeat: the persistent schedule must give the same bits every run.
+    # Repeat: the persistent schedule must give the same bits every run, and
+    # the cp.async and register-path fills the same bits as the TMA fill.
     C2 = pg.gemm_bf16(Ad, Bd)
     assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
+    for fill, stages in (("cpasync", 4), ("cpasync", 2), ("sync", 1)):
+        C3 = pg.gemm_bf16(Ad, Bd, fill=fill, stages=stages)
+        assert torch.equal(C.view(torch.int32), C3.view(torch.int32)), fill
+    assert pg.device_status()[0] == 0
