@@ -250,7 +250,7 @@ def profiled_traffic(kernel_key: str):
                 sha = line.split(":", 1)[1].strip()
             if line.startswith(f"traffic_bytes_per_launch[{kernel_key}]:"):
                 try:
-                    traffic = float(line.split(":", 1)[1].strip())
+                    traffic = float(line.rsplit(":", 1)[1].strip())
                 except ValueError:
                     traffic = None
     if sha is None or sha != kernel_sources_sha():
