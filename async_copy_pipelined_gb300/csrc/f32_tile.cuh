@@ -61,7 +61,7 @@ struct F32Tile {
 // on CUDA async memcpy", section "Real world example" (M = N = 32, long K,
 // one block of one warp), where the fill rather than the FMAs sets the pace.
 using TileXS = F32Tile<32, 32, 8, 4, 8, 8>;
-using TileS = F32Tile<64, 64, 4, 4, 2, 2>;   // the lesson's 64x64x16, 4x4, 256 threads
+using TileS = F32Tile<64, 64, 4, 4, 3, 3>;   // the lesson's 64x64x16, 4x4, 256 threads
 using TileL = F32Tile<128, 128, 8, 8, 1, 1>; // 128x128x16, 8x8, 256 threads
 
 // CTA -> tile.  CTAs are dispatched in linear order (x fastest); walking

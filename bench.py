@@ -494,6 +494,29 @@ def run_ours(args, dist: Dist):
                 v["t_sync_over_t"] = tall["sync/S1/T32"]["us"] / v["us"]
             extras["tallk_32x32x65536"] = tall
             del Atd, Btd, Ctd
+            # Every fill on the other FP32 workloads (the library's automatic
+            # tile choice; TMA reads the ragged A repacked at lda = 1004).
+            from async_copy_pipelined_gb300 import inputs as _inputs
+            per_cfg = {}
+            for wname in ("f32_256", "f32_1024", "f32_ragged"):
+                wc, Ac, Bc = load_workload(wname)
+                Acd, Bcd = to_device(Ac, wc["K"], dev), to_device(Bc, wc["N"], dev)
+                A4d = Acd
+                if wc["lda"] % 4:
+                    A4d = to_device(_inputs.workload_operands(wname, lda=(wc["lda"] + 3) // 4 * 4)[0], wc["K"], dev)
+                Ccd = torch.empty((wc["M"], wc["N"]), dtype=torch.float32, device=dev)
+                fc = 2.0 * wc["M"] * wc["N"] * wc["K"]
+                row = {}
+                for f, s in (("sync", 1), ("cpasync", 2), ("cpasync_mbar", 2), ("tma", 2), ("tma", 4)):
+                    c = gemm_call(pg, wname, A4d if f == "tma" else Acd, Bcd, Ccd, f, s, 0)
+                    mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                    launches += args.sweep_launches
+                    row[f"{f}/S{s}"] = {"tflops": fc / (mean / 1e3) / 1e12, "us": mean * 1e3}
+                for v in row.values():
+                    v["t_sync_over_t"] = row["sync/S1"]["us"] / v["us"]
+                per_cfg[wname] = row
+                del Acd, Bcd, A4d, Ccd
+            extras["fills_per_workload"] = per_cfg
             # BF16 tensor-core leg at its own full size.
             wb, Ab, Bb = load_workload("bf16_8192")
             Abd, Bbd = to_device(Ab, wb["K"], dev), to_device(Bb, wb["N"], dev)
