@@ -71,7 +71,17 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
     for (int f = 0; f < S - 1 && f < k_slices; ++f)
         issue(f);
 
-    for (int kt = 0; kt < k_slices; ++kt) {
+    auto wait_full = [&](int kt) {
+        const bool landed = mbar_wait_bounded(full_bar(kt), parity(kt), p.wait_limit_ns);
+        if (__all_sync(0xffffffffu, landed))
+            return true;
+        if (lane == 0)
+            record_error(p.status, kErrFamilyF32CpAsyncMbar | kErrRoleConsumer);
+        return false;
+    };
+    FragPipe<T> frag;
+    bool chained = false; // slice kt already waited for and its k = 0 fragments loaded
+    for (int kt = 0; kt < k_slices && ok; ++kt) {
         const int fetch = kt + S - 1;
         if (fetch < k_slices) {
             // The stage was last used by slice kt-1: wait until every warp released it.
@@ -84,15 +94,23 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
             }
             issue(fetch);
         }
-        const bool landed = mbar_wait_bounded(full_bar(kt), parity(kt), p.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, landed)) {
-            if (lane == 0)
-                record_error(p.status, kErrFamilyF32CpAsyncMbar | kErrRoleConsumer);
-            ok = false;
-            break;
-        }
         const float *sA = stage0 + (kt % S) * T::kStageFloats;
-        compute_tile<T>(sA, sA + T::kAFloats, tr, tc, acc);
+        if (!chained) {
+            if (!wait_full(kt)) {
+                ok = false;
+                break;
+            }
+            frag.prime(sA, sA + T::kAFloats, tr, tc);
+        }
+        chained = frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() -> const float * {
+            if (!T::kChainSlices || kt + 1 >= k_slices)
+                return nullptr;
+            if (!wait_full(kt + 1)) {
+                ok = false;
+                return nullptr;
+            }
+            return stage0 + ((kt + 1) % S) * T::kStageFloats;
+        }) != nullptr;
         __syncwarp();
         if (lane == 0)
             mbar_arrive(empty_bar(kt));

@@ -85,18 +85,39 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
     Accum<T> acc;
     acc.zero();
 
-    for (int kt = 0; kt < k_slices; ++kt) {
+    auto stage_of = [&](int kt) { return stage0 + (kt % S) * T::kStageFloats; };
+    auto wait_full = [&](int kt) {
         const bool ok = ring.consumer_wait(kt, p.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0)
-                record_error(p.status, kErrFamilyF32Tma | kErrRoleConsumer);
-            return;
+        if (__all_sync(0xffffffffu, ok))
+            return true;
+        if (lane == 0)
+            record_error(p.status, kErrFamilyF32Tma | kErrRoleConsumer);
+        return false;
+    };
+    FragPipe<T> frag;
+    bool chained = false; // slice kt's full barrier already waited and its k = 0 fragments loaded
+    bool failed = false;
+    for (int kt = 0; kt < k_slices; ++kt) {
+        const float *sA = stage_of(kt);
+        if (!chained) {
+            if (!wait_full(kt))
+                return;
+            frag.prime(sA, sA + T::kAFloats, tr, tc);
         }
-        const float *sA = stage0 + (kt % S) * T::kStageFloats;
-        compute_tile<T>(sA, sA + T::kAFloats, tr, tc, acc);
+        chained = frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() -> const float * {
+            if (!T::kChainSlices || kt + 1 >= k_slices)
+                return nullptr;
+            if (!wait_full(kt + 1)) {
+                failed = true;
+                return nullptr;
+            }
+            return stage_of(kt + 1);
+        }) != nullptr;
         __syncwarp();
         if (lane == 0)
             ring.consumer_release(kt);
+        if (failed)
+            return;
     }
 
     store_tile<T>(p, m0, n0, tr, tc, acc);
