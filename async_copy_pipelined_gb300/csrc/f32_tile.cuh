@@ -37,9 +37,11 @@ struct F32Tile {
     // sub-partition's 16K registers.
     static constexpr int kMinBlocks = MIN_BLOCKS_;
     static constexpr int kMinBlocksTma = MIN_BLOCKS_TMA_;
-    // Whether the mbarrier-driven consumers (TMA, cp.async + mbarrier) chain
-    // slices (FragPipe).  Measured at 4096^3: +2.6 % for the 128 tile, -3 %
-    // for the register-tight 64 tile, which therefore runs slice by slice.
+    // Whether the TMA consumers chain slices (FragPipe).  Measured on GB300:
+    // +1 to 4 % for the 128 tile at 4096^3; slower for the register-tight 64
+    // tile and for the one-warp 32 tile of the latency-bound tall-K shape
+    // (there a warp that waits early for slice kt+1 has nothing to hide it
+    // behind), which therefore run slice by slice.
     static constexpr bool kChainSlices = CHAIN_;
     static constexpr int kThreadCols = BN / TN;
     static constexpr int kThreadRows = BM / TM;
@@ -64,7 +66,7 @@ struct F32Tile {
 // One warp, 32x32 tile, 8x4 micro-tile: the latency-bound shape of "A study
 // on CUDA async memcpy", section "Real world example" (M = N = 32, long K,
 // one block of one warp), where the fill rather than the FMAs sets the pace.
-using TileXS = F32Tile<32, 32, 8, 4, 8, 8, true>;
+using TileXS = F32Tile<32, 32, 8, 4, 8, 8, false>;
 using TileS = F32Tile<64, 64, 4, 4, 3, 3, false>;   // the lesson's 64x64x16, 4x4, 256 threads
 using TileL = F32Tile<128, 128, 8, 8, 1, 1, true>; // 128x128x16, 8x8, 256 threads
 
@@ -158,11 +160,13 @@ __device__ __forceinline__ void load_b_frag(const float *__restrict__ sB, int tc
 // A fragment of the next four k are loaded while the FMAs of k run, so
 // shared-memory latency hides behind 32 paired FMAs per k.  They also live
 // across slices: prime() loads k = 0 of the first slice, and run() computes
-// one slice and, during its last k, asks `next` for the following slice's
-// stage (nullptr if there is none or it is not to be chained) and loads that
-// slice's k = 0 fragments into the buffers k = 16 would use.  A consumer that
-// waits for the next slice inside `next` thus overlaps the wait and the first
-// shared loads of slice kt+1 with the FMAs of slice kt.
+// one slice.  At the start of its last k every shared-memory read of the
+// slice has been issued, so run() calls `release` (the stage may be refilled)
+// and then asks `next` for the following slice's stage (nullptr if there is
+// none or it is not to be chained) and loads that slice's k = 0 fragments
+// into the buffers k = 16 would use.  A consumer that waits for the next slice
+// inside `next` thus overlaps the wait and the first shared loads of slice
+// kt+1 with the FMAs of slice kt, without holding slice kt's stage.
 template <class T>
 struct FragPipe {
     float4 a[2][T::TM];
@@ -174,9 +178,9 @@ struct FragPipe {
         load_b_frag<T>(sB, tc, 0, b[0]);
     }
 
-    template <class Next>
+    template <class Release, class Next>
     __device__ __forceinline__ const float *run(const float *__restrict__ sA, const float *__restrict__ sB, int tr,
-                                                int tc, Accum<T> &acc, Next &&next)
+                                                int tc, Accum<T> &acc, Release &&release, Next &&next)
     {
         const float *nA = nullptr;
 #pragma unroll
@@ -188,6 +192,7 @@ struct FragPipe {
             if (k + 1 < T::BK)
                 load_b_frag<T>(sB, tc, k + 1, b[bb ^ 1]);
             if (k + 1 == T::BK) {
+                release();
                 nA = next();
                 if (nA) {
                     load_a_frag<T>(nA, tr, 0, a[ab ^ 1]);
@@ -216,7 +221,7 @@ __device__ __forceinline__ void compute_tile(const float *__restrict__ sA, const
 {
     FragPipe<T> frag;
     frag.prime(sA, sB, tr, tc);
-    frag.run(sA, sB, tr, tc, acc, []() -> const float * { return nullptr; });
+    frag.run(sA, sB, tr, tc, acc, []() {}, []() -> const float * { return nullptr; });
 }
 
 // Four consecutive elements (r, c..c+3) of an R x C row-major matrix with

@@ -80,7 +80,6 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
         return false;
     };
     FragPipe<T> frag;
-    bool chained = false; // slice kt already waited for and its k = 0 fragments loaded
     for (int kt = 0; kt < k_slices && ok; ++kt) {
         const int fetch = kt + S - 1;
         if (fetch < k_slices) {
@@ -94,26 +93,19 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
             }
             issue(fetch);
         }
-        const float *sA = stage0 + (kt % S) * T::kStageFloats;
-        if (!chained) {
-            if (!wait_full(kt)) {
-                ok = false;
-                break;
-            }
-            frag.prime(sA, sA + T::kAFloats, tr, tc);
+        if (!wait_full(kt)) {
+            ok = false;
+            break;
         }
-        chained = frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() -> const float * {
-            if (!T::kChainSlices || kt + 1 >= k_slices)
-                return nullptr;
-            if (!wait_full(kt + 1)) {
-                ok = false;
-                return nullptr;
-            }
-            return stage0 + ((kt + 1) % S) * T::kStageFloats;
-        }) != nullptr;
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(empty_bar(kt));
+        const float *sA = stage0 + (kt % S) * T::kStageFloats;
+        frag.prime(sA, sA + T::kAFloats, tr, tc);
+        // Slice by slice: waiting early for slice kt+1 measured slower here,
+        // since the same warps must first issue that slice's copies.
+        frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() {
+            __syncwarp(); // every lane's reads of the stage precede the release
+            if (lane == 0)
+                mbar_arrive(empty_bar(kt));
+        }, []() -> const float * { return nullptr; });
     }
     cp_async_wait_all(); // none of this thread's copies may land after it exits
 

@@ -104,7 +104,11 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
                 return;
             frag.prime(sA, sA + T::kAFloats, tr, tc);
         }
-        chained = frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() -> const float * {
+        chained = frag.run(sA, sA + T::kAFloats, tr, tc, acc, [&]() {
+            __syncwarp(); // every lane's reads of the stage precede the release
+            if (lane == 0)
+                ring.consumer_release(kt);
+        }, [&]() -> const float * {
             if (!T::kChainSlices || kt + 1 >= k_slices)
                 return nullptr;
             if (!wait_full(kt + 1)) {
@@ -113,9 +117,6 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
             }
             return stage_of(kt + 1);
         }) != nullptr;
-        __syncwarp();
-        if (lane == 0)
-            ring.consumer_release(kt);
         if (failed)
             return;
     }
