@@ -1,7 +1,7 @@
 """GPU parity of the BF16 tensor-core path against the oracle, through the C ABI.
 
 The tensor core sums in its own order, so results are compared with the
-exact-product float64 oracle within a tolerance: the benchmark spec's bound
+exact-product float64 oracle within a tolerance: the acceptance bound
 ||C - C_ref||_F / ||C_ref||_F <= 2e-2, and the much tighter per-element bound
 |C - C_ref| <= K * 2^-22 * sum_k |a_ik b_kj| that float32 accumulation of
 exact products satisfies.  Small-integer inputs and the identity / all-ones

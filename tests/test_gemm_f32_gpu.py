@@ -1,6 +1,6 @@
 """GPU parity of the FP32 kernel family against the oracle, through the C ABI.
 
-The bar (north star of the library): every FP32 result equals the oracle's
+The bar: every FP32 result equals the oracle's
 float32 FMA chain bit for bit (hence all fills, stage counts and tiles are
 bit-identical to each other, the pages' memcmp invariant), and lies within
 max|C - C_ref| <= 1e-5 * K of the float64 definition.

@@ -206,7 +206,7 @@ def test_fmaf_chain_within_recursive_summation_bound(orc, K):
     u = 2.0 ** -24
     gamma = K * u / (1 - K * u)
     assert np.all(np.abs(chain - exact) <= gamma * absum)
-    # The spec acceptance form, max|C - C_ref| <= 1e-5 * K, holds too.
+    # The library's acceptance bound for FP32, max|C - C_ref| <= 1e-5 * K, holds too.
     assert np.max(np.abs(chain - exact)) <= 1e-5 * K
 
 
