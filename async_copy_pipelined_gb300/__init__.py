@@ -152,17 +152,53 @@ def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, a_ptr
     return p.as_dict()
 
 
+# Host-buffer calls move A and C in row chunks of at least this many rows.
+HOST_CHUNK_MIN_ROWS = 1024
+HOST_CHUNKS_MAX = 4
+
+
+def host_row_chunks(M: int):
+    """Row ranges [r0, r1) the host-buffer path splits A and C into: up to
+    HOST_CHUNKS_MAX chunks of at least HOST_CHUNK_MIN_ROWS rows, each a whole
+    number of 128-row tiles except the last."""
+    n = max(1, min(HOST_CHUNKS_MAX, M // HOST_CHUNK_MIN_ROWS))
+    rows = -(-M // n)
+    rows = -(-rows // 128) * 128
+    return [(r0, min(M, r0 + rows)) for r0 in range(0, M, rows)]
+
+
 def _host_roundtrip(fn, A, B, C, dtype_out):
-    """Host tensors: pinned H2D copies, the device call, D2H copy of C."""
+    """Host tensors in, host C out.
+
+    B is copied to the device once.  A and C then move in row chunks on two
+    alternating streams, so the host-to-device copy of one chunk, the GEMM of
+    another and the device-to-host copy of a third overlap.  Each C element
+    is computed from the same row of A, the same B and the same kernel
+    arithmetic as in a single call, so chunking changes no result bit.  Host
+    tensors should be pinned for the copies to be asynchronous.  Returns after
+    C has been written."""
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
-    Ad = A.to(dev, non_blocking=True)
-    Bd = B.to(dev, non_blocking=True)
-    Cd = fn(Ad, Bd, None)
+    M, N = A.shape[0], B.shape[1]
     if C is None:
-        C = torch.empty(Cd.shape, dtype=dtype_out, pin_memory=True)
-    C.copy_(Cd, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+        C = torch.empty((M, N), dtype=dtype_out, pin_memory=True)
+    cur = torch.cuda.current_stream(dev)
+    Bd = B.to(dev, non_blocking=True)
+    b_ready = torch.cuda.Event()
+    b_ready.record(cur)
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    for i, (r0, r1) in enumerate(host_row_chunks(M)):
+        s = streams[i % 2]
+        s.wait_event(b_ready)
+        with torch.cuda.stream(s):
+            # Allocated on stream s, so the caching allocator reuses these
+            # blocks only in s's order once they are released.
+            Ad = A[r0:r1].to(dev, non_blocking=True)
+            Cd = fn(Ad, Bd, s)
+            C[r0:r1].copy_(Cd, non_blocking=True)
+    for s in streams:
+        cur.wait_stream(s)
+    cur.synchronize()
     return C
 
 
@@ -172,12 +208,14 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     A (M x K), B (K x N) float32 tensors; C (M x N) float32 output, allocated
     if None.  CUDA tensors run on the device asynchronously on `stream`
     (default: torch's current stream).  CPU tensors are copied to the current
-    device, computed, and copied back (the end-to-end path).
+    device, computed and copied back, with the copies of row chunks
+    overlapping the GEMMs of others (see _host_roundtrip); the call returns
+    once C is on the host.
     """
     import torch
     if not A.is_cuda:
-        return _host_roundtrip(lambda a, b, _c: gemm_f32(a, b, None, fill=fill, stages=stages,
-                                                         block_tile=block_tile, stream=stream),
+        return _host_roundtrip(lambda a, b, s: gemm_f32(a, b, None, fill=fill, stages=stages,
+                                                        block_tile=block_tile, stream=s),
                                A, B, C, torch.float32)
     if A.dtype != torch.float32 or B.dtype != torch.float32:
         raise TypeError("gemm_f32 takes float32 tensors")
@@ -203,7 +241,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
     the MMAs read; all three give the same bits."""
     import torch
     if not A.is_cuda:
-        return _host_roundtrip(lambda a, b, _c: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=stream),
+        return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=s),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")

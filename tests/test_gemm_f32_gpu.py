@@ -242,6 +242,33 @@ def test_non_default_stream():
     assert_bitwise_equal(C.cpu().numpy(), oracle.gemm_fmaf_chain(A, B, M, N, K), "side stream")
 
 
+def test_host_row_chunks_cover_rows_once():
+    import async_copy_pipelined_gb300 as pg
+    for M in (1, 127, 1023, 1024, 2048, 2500, 4096, 9000):
+        ch = pg.host_row_chunks(M)
+        assert ch[0][0] == 0 and ch[-1][1] == M
+        assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))
+        assert all((r1 - r0) % 128 == 0 for r0, r1 in ch[:-1])
+        assert len(ch) <= pg.HOST_CHUNKS_MAX
+
+
+@pytest.mark.parametrize("fill", ["sync", "tma"])
+def test_host_tensors_chunked_match_device_path(fill):
+    """A host call large enough to be split into row chunks on two streams
+    gives the same bits as one device call."""
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    M, N, K = 2500, 384, 256
+    A, B = f32_operands("uniform", M, N, K, seed=10, fill="tma")
+    Ah = torch.from_numpy(A).pin_memory()[:, :K]
+    Bh = torch.from_numpy(B).pin_memory()[:, :N]
+    assert len(pg.host_row_chunks(M)) > 1
+    Ch = pg.gemm_f32(Ah, Bh, fill=fill)
+    Cd = pg.gemm_f32(torch.from_numpy(A).cuda()[:, :K], torch.from_numpy(B).cuda()[:, :N], fill=fill)
+    assert torch.equal(Ch.view(torch.int32), Cd.cpu().view(torch.int32))
+    assert_bitwise_equal(Ch.numpy(), oracle.gemm_fmaf_chain(A, B, M, N, K), "chunked host path")
+
+
 def test_host_tensors_end_to_end():
     import torch
     import async_copy_pipelined_gb300 as pg
