@@ -10,6 +10,8 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import contextlib
+import fcntl
 import glob
 import os
 import shutil
@@ -61,10 +63,28 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stderr
 
 
+@contextlib.contextmanager
+def _build_lock():
+    """One build at a time per tree (several ranks of one job may call build())."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(OUT_DIR, exist_ok=True)
+    with _build_lock():
+        if not force and up_to_date():  # another process built it while we waited
+            return LIB_PATH
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose: bool) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         results = list(ex.map(_compile, srcs))

@@ -45,11 +45,25 @@ def compile_source(src: str, out: str) -> str:
     return out
 
 
+def _fresh() -> bool:
+    return os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C, OpenMP, no fast-math)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+    """Compile the oracle with gcc (plain C, OpenMP, no fast-math); one build
+    at a time per tree."""
+    if not force and _fresh():
         return _LIB_PATH
-    return compile_source(_SRC, _LIB_PATH)
+    import fcntl
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    with open(_LIB_PATH + ".lock", "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            if force or not _fresh():
+                compile_source(_SRC, _LIB_PATH)
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+    return _LIB_PATH
 
 
 def load_variant(path: str):
