@@ -123,3 +123,16 @@ def test_workload_8192_sampled():
         C3 = pg.gemm_bf16(Ad, Bd, fill=fill, stages=stages)
         assert torch.equal(C.view(torch.int32), C3.view(torch.int32)), fill
     assert pg.device_status()[0] == 0
+
+
+@pytest.mark.parametrize("fill,stages", [("tma", 4), ("tma", 2), ("cpasync", 3), ("sync", 1)])
+def test_randomized_shapes(fill, stages):
+    """Random ragged sizes and padded leading dimensions (seeded)."""
+    rng = np.random.default_rng(1234 + stages)
+    for _ in range(8):
+        M, N, K = (int(rng.integers(1, 400)), int(rng.integers(1, 600)), int(rng.integers(1, 300)))
+        A, B = bf16_operands("normal", M, N, K, M + N + K, lda=K + int(rng.integers(0, 17)),
+                             ldb=N + int(rng.integers(0, 17)))
+        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+        want = oracle.gemm_bf16_f64(A, B, M, N, K)
+        _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} {M}x{N}x{K}")

@@ -5,6 +5,8 @@ float32 FMA chain bit for bit (hence all fills, stage counts and tiles are
 bit-identical to each other, the pages' memcmp invariant), and lies within
 max|C - C_ref| <= 1e-5 * K of the float64 definition.
 """
+import zlib
+
 import numpy as np
 import pytest
 
@@ -277,3 +279,32 @@ def test_host_tensors_end_to_end():
     C = pg.gemm_f32(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), fill="cpasync")
     assert not C.is_cuda
     assert_bitwise_equal(C.numpy(), oracle.gemm_fmaf_chain(A, B, M, N, K), "host round trip")
+
+
+# ----------------------------------------------------- randomized shapes
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        M = int(rng.integers(1, 300))
+        N = int(rng.integers(1, 300))
+        K = int(rng.integers(1, 200))
+        pad_a = int(rng.integers(0, 9))
+        pad_b = int(rng.integers(0, 9))
+        cases.append((M, N, K, pad_a, pad_b))
+    return cases
+
+
+@pytest.mark.parametrize("fill,stages,tile", [("sync", 1, 64), ("sync", 1, 128), ("cpasync", 3, 64),
+                                              ("cpasync", 5, 128), ("cpasync_mbar", 2, 32),
+                                              ("cpasync_mbar", 4, 128), ("tma", 2, 32), ("tma", 3, 64),
+                                              ("tma", 6, 128)])
+def test_randomized_shapes(fill, stages, tile):
+    """Random ragged sizes and leading-dimension padding, every result bitwise
+    equal to the oracle's FMA chain (seeded, so failures reproduce)."""
+    for M, N, K, pad_a, pad_b in _random_cases(12, seed=zlib.crc32(f"{fill}/{stages}/{tile}".encode())):
+        A, B = f32_operands("normal", M, N, K, seed=M * 7 + N * 3 + K, lda=K + pad_a, ldb=N + pad_b, fill=fill)
+        got, _ = run_f32(A, B, M, N, K, fill, stages, tile)
+        assert_bitwise_equal(got, oracle.gemm_fmaf_chain(A, B, M, N, K),
+                             f"{fill}/S{stages}/T{tile} {M}x{N}x{K} pads {pad_a},{pad_b}")
