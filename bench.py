@@ -566,7 +566,8 @@ def run_ours(args, dist: Dist):
         e2e = {"value": flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(Ah.element_size() * M * K + Bh.element_size() * K * N),
                "d2h_bytes_per_step": int(4 * M * N), "ms_per_step": e_total / e_steps}
-        launches_e2e = e_steps
+        # One GEMM launch per row chunk of the host path, every step.
+        launches_e2e = e_steps * len(pg.host_row_chunks(M))
 
     kernel_key = f"{name}:{leg['fill']}/S{leg['stages']}/T{leg['tile']}"
     if is_bf16:
@@ -594,9 +595,10 @@ def run_ours(args, dist: Dist):
         "config": workload_config(name, w, {**leg, "gate": gate,
                                             "parallelism": "replicas" if dist.world > 1 else "single GPU"}),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": launches, "gpu_launches_breakdown": {"timed_steps": args.steps,
+        "gpu_launches": launches + (launches_e2e if e2e else 0),
+        "gpu_launches_breakdown": {"timed_steps": args.steps,
                                                              "sweep_and_bf16_legs": launches - args.steps,
-                                                             "e2e_steps": launches_e2e if e2e else 0},
+                                                             "e2e_launches": launches_e2e if e2e else 0},
         "kernel_sources_sha": kernel_sources_sha(),
     }
     line.update(extras)
