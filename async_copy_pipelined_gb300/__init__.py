@@ -152,9 +152,16 @@ def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, a_ptr
     return p.as_dict()
 
 
-# Host-buffer calls move A and C in row chunks of at least this many rows.
-HOST_CHUNK_MIN_ROWS = 1024
-HOST_CHUNKS_MAX = 4
+# Host-buffer calls move A and C in row chunks of at least this many rows,
+# issued round-robin on HOST_STREAMS streams that are created once per device.
+# Measured on GB300 at 4096^3 (FP32, host copies at about 190 GB/s each way):
+# eight 512-row chunks on four streams take 2.74 ms a call, four 1024-row
+# chunks on two streams 2.83 ms, and creating the streams on every call adds
+# about 0.1 ms more.
+HOST_CHUNK_MIN_ROWS = 512
+HOST_CHUNKS_MAX = 16
+HOST_STREAMS = 4
+_host_streams = {}
 
 
 def host_row_chunks(M: int):
@@ -167,16 +174,25 @@ def host_row_chunks(M: int):
     return [(r0, min(M, r0 + rows)) for r0 in range(0, M, rows)]
 
 
+def _streams_for(dev):
+    import torch
+    streams = _host_streams.get(dev.index)
+    if streams is None:
+        streams = _host_streams[dev.index] = [torch.cuda.Stream(dev) for _ in range(HOST_STREAMS)]
+    return streams
+
+
 def _host_roundtrip(fn, A, B, C, dtype_out):
     """Host tensors in, host C out.
 
-    B is copied to the device once.  A and C then move in row chunks on two
-    alternating streams, so the host-to-device copy of one chunk, the GEMM of
-    another and the device-to-host copy of a third overlap.  Each C element
-    is computed from the same row of A, the same B and the same kernel
-    arithmetic as in a single call, so chunking changes no result bit.  Host
-    tensors should be pinned for the copies to be asynchronous.  Returns after
-    C has been written."""
+    B is copied to the device once.  A and C then move in row chunks on
+    HOST_STREAMS streams in turn, so the host-to-device copy of one chunk, the
+    GEMMs of others and the device-to-host copy of another overlap, and the
+    GEMM of the next chunk fills the SMs the last wave of the previous one
+    leaves idle.  Each C element is computed from the same row of A, the same
+    B and the same kernel arithmetic as in a single call, so chunking changes
+    no result bit.  Host tensors should be pinned for the copies to be
+    asynchronous.  Returns after C has been written."""
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
     M, N = A.shape[0], B.shape[1]
@@ -186,9 +202,9 @@ def _host_roundtrip(fn, A, B, C, dtype_out):
     Bd = B.to(dev, non_blocking=True)
     b_ready = torch.cuda.Event()
     b_ready.record(cur)
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    streams = _streams_for(dev)
     for i, (r0, r1) in enumerate(host_row_chunks(M)):
-        s = streams[i % 2]
+        s = streams[i % len(streams)]
         s.wait_event(b_ready)
         with torch.cuda.stream(s):
             # Allocated on stream s, so the caching allocator reuses these
@@ -214,6 +230,13 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     """
     import torch
     if not A.is_cuda:
+        if block_tile == 0:
+            # The tile the whole problem would get, not what one row chunk
+            # alone would get.
+            try:
+                block_tile = plan_f32(A.shape[0], B.shape[1], A.shape[1], fill=fill, stages=stages)["block_m"]
+            except (RuntimeError, ValueError):
+                pass  # the chunk calls report the error
         return _host_roundtrip(lambda a, b, s: gemm_f32(a, b, None, fill=fill, stages=stages,
                                                         block_tile=block_tile, stream=s),
                                A, B, C, torch.float32)

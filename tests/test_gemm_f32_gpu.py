@@ -256,15 +256,17 @@ def test_host_row_chunks_cover_rows_once():
 
 @pytest.mark.parametrize("fill", ["sync", "tma"])
 def test_host_tensors_chunked_match_device_path(fill):
-    """A host call large enough to be split into row chunks on two streams
-    gives the same bits as one device call."""
+    """A host call split into more row chunks than it has streams (so every
+    stream runs several chunks, the last one ragged) gives the same bits as
+    one device call."""
     import torch
     import async_copy_pipelined_gb300 as pg
-    M, N, K = 2500, 384, 256
+    M, N, K = 3300, 384, 256
     A, B = f32_operands("uniform", M, N, K, seed=10, fill="tma")
     Ah = torch.from_numpy(A).pin_memory()[:, :K]
     Bh = torch.from_numpy(B).pin_memory()[:, :N]
-    assert len(pg.host_row_chunks(M)) > 1
+    chunks = pg.host_row_chunks(M)
+    assert len(chunks) > pg.HOST_STREAMS and (chunks[-1][1] - chunks[-1][0]) % 128
     Ch = pg.gemm_f32(Ah, Bh, fill=fill)
     Cd = pg.gemm_f32(torch.from_numpy(A).cuda()[:, :K], torch.from_numpy(B).cuda()[:, :N], fill=fill)
     assert torch.equal(Ch.view(torch.int32), Cd.cpu().view(torch.int32))
