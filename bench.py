@@ -283,7 +283,8 @@ def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile):
 
 
 def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
-    """Mean / min ms of `launches` calls, each after an L2 flush, events on the stream."""
+    """Mean / min / median ms of `launches` calls, each after an L2 flush,
+    events on the stream."""
     import torch
     for _ in range(warmup):
         flush()
@@ -296,7 +297,7 @@ def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
         timer.end()
     torch.cuda.synchronize()
     d = timer.durations_ms()
-    return statistics.mean(d), min(d)
+    return statistics.mean(d), min(d), statistics.median(d)
 
 
 # --------------------------------------------------------------------- oracle leg
@@ -325,6 +326,32 @@ def oracle_sample(name: str, A, B, w, seconds: float, gpu_rows=None):
         g = gpu_rows[:rows].astype(np.float64)
         res["max_abs_diff_vs_gpu"] = float(np.max(np.abs(g - out)))
     return res
+
+
+def oracle_small_configs():
+    """The oracle over the whole output of the two small FP32 workloads, on
+    all host cores and on one thread (TFLOP/s and seconds)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    out = {}
+    try:
+        for wname in ("f32_256", "f32_1024"):
+            w, A, B = load_workload(wname)
+            M, N, K = w["M"], w["N"], w["K"]
+            Ac = np.ascontiguousarray(A[:, :K])
+            row = {}
+            for label, n in (("all_cores", cores), ("one_thread", 1)):
+                oracle.set_num_threads(n)
+                t0 = time.perf_counter()
+                oracle.gemm_f64(Ac, B, M, N, K)
+                t = time.perf_counter() - t0
+                row[label] = {"threads": n, "seconds": t, "tflops": 2.0 * M * N * K / t / 1e12}
+            out[wname] = row
+    finally:
+        oracle.set_num_threads(cores)
+    return out
 
 
 def run_reference(args, dist: Dist):
@@ -469,9 +496,10 @@ def run_ours(args, dist: Dist):
                 variants = [v for v in variants if v[0] != "tma"]
             for f, s, t in variants:
                 c = gemm_call(pg, name, Ad, Bd, Cd, f, s, t)
-                mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
                 fills[f"{f}/S{s}/T{t}"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
+                                           "ms_median": med,
                                            "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
             t_sync = fills["sync/S1/T128"]["ms"]
             for v in fills.values():
@@ -487,9 +515,10 @@ def run_ours(args, dist: Dist):
             for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("tma", 2), ("tma", 4), ("cpasync_mbar", 2),
                          ("cpasync_mbar", 4)):
                 c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
-                mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
-                tall[f"{f}/S{s}/T32"] = {"us": mean * 1e3, "gflops": ft / (mean / 1e3) / 1e9}
+                tall[f"{f}/S{s}/T32"] = {"us": mean * 1e3, "us_min": best * 1e3, "us_median": med * 1e3,
+                                         "gflops": ft / (mean / 1e3) / 1e9}
             for v in tall.values():
                 v["t_sync_over_t"] = tall["sync/S1/T32"]["us"] / v["us"]
             extras["tallk_32x32x65536"] = tall
@@ -509,9 +538,10 @@ def run_ours(args, dist: Dist):
                 row = {}
                 for f, s in (("sync", 1), ("cpasync", 2), ("cpasync_mbar", 2), ("tma", 2), ("tma", 4)):
                     c = gemm_call(pg, wname, A4d if f == "tma" else Acd, Bcd, Ccd, f, s, 0)
-                    mean, best = time_kernel(pg, c, flush, args.sweep_launches)
+                    mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                     launches += args.sweep_launches
-                    row[f"{f}/S{s}"] = {"tflops": fc / (mean / 1e3) / 1e12, "us": mean * 1e3}
+                    row[f"{f}/S{s}"] = {"tflops": fc / (mean / 1e3) / 1e12, "us": mean * 1e3,
+                                        "us_min": best * 1e3, "us_median": med * 1e3}
                 for v in row.values():
                     v["t_sync_over_t"] = row["sync/S1"]["us"] / v["us"]
                 per_cfg[wname] = row
@@ -523,10 +553,10 @@ def run_ours(args, dist: Dist):
             Cbd = torch.empty((wb["M"], wb["N"]), dtype=torch.float32, device=dev)
             fb = 2.0 * wb["M"] * wb["N"] * wb["K"]
             cb = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", 4, 0)
-            mean, best = time_kernel(pg, cb, flush, args.sweep_launches)
+            mean, best, med = time_kernel(pg, cb, flush, args.sweep_launches)
             launches += args.sweep_launches
             tf = fb / (mean / 1e3) / 1e12
-            extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "stages": 4,
+            extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "ms_median": med, "stages": 4,
                                    "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak,
                                                 "unit": UNIT, "frac": tf / bf16_peak,
                                                 "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"},
@@ -534,9 +564,9 @@ def run_ours(args, dist: Dist):
             bfills = {}
             for f, s in (("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 4), ("sync", 1)):
                 c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, f, s, 0)
-                m2, b2 = time_kernel(pg, c, flush, args.sweep_launches)
+                m2, b2, md2 = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
-                bfills[f"{f}/S{s}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2}
+                bfills[f"{f}/S{s}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2, "ms_median": md2}
             for v in bfills.values():
                 v["t_sync_over_t"] = bfills["sync/S1"]["ms"] / v["ms"]
             extras["bf16_8192"]["fills"] = bfills
@@ -586,10 +616,14 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0 and not args.no_cpu_baseline:
         gpu_rows = Cd[: min(M, 4096)].cpu().numpy()
         cpu = oracle_sample(name, A, B, w, args.cpu_seconds, gpu_rows=gpu_rows)
+        if not is_bf16:
+            cpu["small_configs"] = oracle_small_configs()
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step,
+        "step_ms": {"mean": local_mean, "median": statistics.median(per), "min": min(per)},
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in, f32 accumulate" if is_bf16 else "f32",
         "data": "synthetic (seeded SplitMix64 operands, see async_copy_pipelined_gb300/inputs.py)",
         "config": workload_config(name, w, {**leg, "gate": gate,
