@@ -125,6 +125,20 @@ def test_workload_8192_sampled():
     assert pg.device_status()[0] == 0
 
 
+def test_workload_8192_smallint_exact_sampled():
+    """Entries in {-2..2} at 8192^3: exact in bfloat16, and every partial sum
+    is an integer of magnitude at most 4K < 2^24, so the FP32 accumulator is
+    exact whatever order the tensor cores add in.  Sampled rows (every
+    column) must equal the exact product, for every fill."""
+    M = N = K = 8192
+    A, B = bf16_operands("smallint", M, N, K, 104)
+    rows = sample_rows(M, 24, seed=104, tiles=(128,))
+    want = oracle_bf16_rows(A, B, rows, N, K).astype(np.float32)
+    for fill, stages in (("tma", 4), ("cpasync", 4), ("sync", 1)):
+        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+        np.testing.assert_array_equal(got[rows], want, err_msg=f"8192^3 small-int {fill}/S{stages}")
+
+
 @pytest.mark.parametrize("fill,stages", [("tma", 4), ("tma", 2), ("cpasync", 3), ("sync", 1)])
 def test_randomized_shapes(fill, stages):
     """Random ragged sizes and padded leading dimensions (seeded)."""

@@ -12,7 +12,7 @@ import pytest
 
 from async_copy_pipelined_gb300 import inputs
 from gpu_util import (F32_VARIANTS, assert_bitwise_equal, f32_operands, oracle_f64_rows, oracle_fmaf_rows,
-                      run_f32, sample_rows)
+                      run_f32, sample_rows, tma_pitch)
 
 import oracle
 
@@ -177,6 +177,27 @@ def test_workload_ragged_lda_k_plus_3():
     got = ref.cpu().numpy()[rows]
     assert_bitwise_equal(got, oracle_fmaf_rows(A, B, rows, N, K), "ragged sampled rows")
     assert np.max(np.abs(got - oracle_f64_rows(A, B, rows, N, K))) <= 1e-5 * K
+
+
+# ----------------------------------------------------- small integers at every workload's shape
+
+@pytest.mark.parametrize("name", ["f32_256", "f32_1024", "f32_4096", "f32_ragged"])
+def test_workload_shapes_smallint_exact(name):
+    """Entries in {-2..2} at the workload's own sizes and leading dimension.
+    Every partial sum is an integer of magnitude at most 4K < 2^24, so the
+    product is exact in any order: every fill must equal the exact product
+    over the whole output (the TMA fill reads the same values at the next
+    16-byte row pitch when lda is not one)."""
+    w = inputs.WORKLOADS[name]
+    M, N, K, lda = w["M"], w["N"], w["K"], w["lda"]
+    seed = 100 + w["seed"]
+    A = inputs.matrix_f32("smallint", M, K, seed, inputs.TAG_A, ld=lda)
+    B = inputs.matrix_f32("smallint", K, N, seed, inputs.TAG_B)
+    A4 = A if lda % 4 == 0 else inputs.matrix_f32("smallint", M, K, seed, inputs.TAG_A, ld=tma_pitch(lda))
+    want = oracle.gemm_f64(A, B, M, N, K).astype(np.float32)
+    for fill, stages in (("sync", 1), ("cpasync", 3), ("cpasync_mbar", 4), ("tma", 4)):
+        got, _ = run_f32(A4 if fill == "tma" else A, B, M, N, K, fill, stages, 0)
+        np.testing.assert_array_equal(got, want, err_msg=f"{name} {fill}/S{stages}")
 
 
 # ----------------------------------------------------- tall K, one warp
