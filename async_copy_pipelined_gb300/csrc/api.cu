@@ -133,10 +133,19 @@ int f32_smem_bytes(int tile, int fill, int stages)
 }
 
 
+// The tensor-core kernel is persistent (one CTA per SM) and allocates all of
+// an SM's tensor memory, so a second CTA placed on the same SM would block in
+// tcgen05.alloc until the first had finished every tile while another SM sat
+// idle.  Small rings (two stages, or the one-stage register fill) would leave
+// room for a second CTA; the request is raised so that two never fit in an
+// SM's 228 KB.
+constexpr int kBf16ExclusiveSmemBytes = 116 * 1024;
+
 int bf16_smem_bytes(int stages)
 {
     const int stage_bytes = (kBf16BlockM * kBf16BlockK + kBf16BlockK * kBf16BlockN) * 2;
-    return stages * stage_bytes + 1024 /* barriers, TMEM slot */ + 1024 /* alignment slack */;
+    const int need = stages * stage_bytes + 1024 /* barriers, TMEM slot */ + 1024 /* alignment slack */;
+    return need > kBf16ExclusiveSmemBytes ? need : kBf16ExclusiveSmemBytes;
 }
 
 // ------------------------------------------------------------ planning
