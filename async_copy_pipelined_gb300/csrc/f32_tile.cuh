@@ -302,6 +302,25 @@ __device__ __forceinline__ void issue_slice_cpasync(float *stage, const F32Args 
     float *sA = stage;
     float *sB = stage + T::kAFloats;
     const int k0 = kt * T::BK;
+    if (p.a_vec && p.b_vec && m0 + T::BM <= p.M && n0 + T::BN <= p.N && k0 + T::BK <= p.K) {
+        // Interior slice with 16-byte rows: every chunk is a whole in-range
+        // 16-byte copy, so no guard and no source size are needed.
+#pragma unroll
+        for (int q = 0; q < T::kAChunksPerThread; ++q) {
+            const int c = tid + q * T::kThreads;
+            int r, k;
+            a_chunk_coords<T>(c, m0, k0, r, k);
+            cp_async_cg16_full(smem_u32(sA + 4 * c), p.A + static_cast<long long>(r) * p.lda + k);
+        }
+#pragma unroll
+        for (int q = 0; q < T::kBChunksPerThread; ++q) {
+            const int c = tid + q * T::kThreads;
+            int k, n;
+            b_chunk_coords<T>(c, k0, n0, k, n);
+            cp_async_cg16_full(smem_u32(sB + 4 * c), p.B + static_cast<long long>(k) * p.ldb + n);
+        }
+        return;
+    }
 #pragma unroll
     for (int q = 0; q < T::kAChunksPerThread; ++q) {
         const int c = tid + q * T::kThreads;

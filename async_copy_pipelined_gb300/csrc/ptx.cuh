@@ -27,6 +27,12 @@ __device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
+// 16-byte copy of an in-range chunk (no source-size operand).
+__device__ __forceinline__ void cp_async_cg16_full(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
 // 4-byte copy (.ca: the only cache qualifier allowed below 16 bytes).
 __device__ __forceinline__ void cp_async_ca4(uint32_t dst, const void *src, uint32_t src_bytes)
 {
