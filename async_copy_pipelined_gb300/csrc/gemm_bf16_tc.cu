@@ -22,12 +22,17 @@
 // The fills, as in the FP32 family ("Day 74: Async copies and pipelines", day
 // 80's goal of this pipeline feeding tensor cores):
 //   TMA       as above: one thread, one descriptor per box.
-//   cp.async  four producer warps copy 16-byte chunks straight into the
-//             swizzled stage with cp.async, keep one stage in flight per
-//             thread (wait_group 1), and mark a stage full once their own
-//             copies of it have landed.
-//   sync      four producer warps load chunks into registers and store them
-//             into the one and only stage; loads and MMAs strictly alternate.
+//   cp.async  sixteen producer warps copy 16-byte chunks straight into the
+//             swizzled stage with cp.async (interior stages without guards),
+//             keep S-1 stages in flight per thread (wait_group S-2), and mark
+//             a stage full once their own copies of it have landed.  One
+//             thread cannot issue 3072 copies per stage fast enough, so the
+//             copy issue is spread over 512 threads; measured on GB300 at
+//             8192^3, S = 4: 268 TFLOP/s with four warps and one stage in
+//             flight, 675 with eight warps, 834 with sixteen.
+//   sync      the same sixteen warps load chunks into registers and store
+//             them into the one and only stage; loads and MMAs strictly
+//             alternate.
 // The cp.async and sync producers write the 128-byte-swizzled layout the TMA
 // would write (16-byte chunk index XOR row mod 8 within each 1024-byte atom)
 // through the generic proxy; each writer issues fence.proxy.async before its
@@ -65,7 +70,7 @@ constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 KiB
 constexpr uint32_t kTmemCols = 2 * BN;                     // two accumulators
 constexpr int kGroupM = 16;
 constexpr int kStageChunks = kStageBytes / 16;           // 3072 16-byte chunks per stage
-constexpr int kCopyWarps = 4;                             // cp.async / sync producer warps
+constexpr int kCopyWarps = 16;                            // cp.async / sync producer warps
 constexpr int kCopyThreads = kCopyWarps * 32;
 
 template <int Fill>
@@ -238,6 +243,12 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
     } else if (Fill != GEMM_FILL_TMA && warp < R::kProducerWarps) {
         // ------------------------------------------- cp.async / sync producers
         const int ptid = threadIdx.x;
+        // Stages of copies each thread keeps in flight beyond the one it has
+        // just issued: the full barrier of stage f is arrived on kLag stages
+        // later, once this thread's copies of it have landed.  The producer
+        // acquiring stage f needs stage f - S released, whose arrival came
+        // at stage f - S + kLag, so kLag <= S - 1 cannot deadlock.
+        constexpr int kLag = S >= 3 ? S - 2 : 1;
         int f = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -253,30 +264,49 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                 }
                 const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
                 if constexpr (Fill == GEMM_FILL_CPASYNC) {
-                    for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
-                        int grow, gcol;
-                        bool is_a;
-                        uint32_t off;
-                        stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
-                        const uint16_t *gbase = is_a ? p.A : p.B;
-                        const long long ld = is_a ? p.lda : p.ldb;
-                        const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
-                        uint32_t nbytes = 0;
-                        const uint16_t *src = gbase;
-                        if (grow < rows && gcol < cols) {
-                            nbytes = static_cast<uint32_t>(min(cols - gcol, 8)) * 2u;
-                            src = gbase + static_cast<long long>(grow) * ld + gcol;
+                    const bool interior = (mb + 1) * BM <= p.M && (nb + 1) * BN <= p.N && (kb + 1) * BK <= p.K;
+                    if (interior) {
+                        // Every chunk is a whole in-range 16-byte copy (the
+                        // planner requires 16-byte row pitches).
+                        for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
+                            int grow, gcol;
+                            bool is_a;
+                            uint32_t off;
+                            stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
+                            const uint16_t *src = is_a ? p.A + static_cast<long long>(grow) * p.lda + gcol
+                                                       : p.B + static_cast<long long>(grow) * p.ldb + gcol;
+                            cp_async_cg16_full(dst + off, src);
                         }
-                        cp_async_cg16(dst + off, src, nbytes);
+                    } else {
+                        for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
+                            int grow, gcol;
+                            bool is_a;
+                            uint32_t off;
+                            stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
+                            const uint16_t *gbase = is_a ? p.A : p.B;
+                            const long long ld = is_a ? p.lda : p.ldb;
+                            const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
+                            uint32_t nbytes = 0;
+                            const uint16_t *src = gbase;
+                            if (grow < rows && gcol < cols) {
+                                nbytes = static_cast<uint32_t>(min(cols - gcol, 8)) * 2u;
+                                src = gbase + static_cast<long long>(grow) * ld + gcol;
+                            }
+                            cp_async_cg16(dst + off, src, nbytes);
+                        }
                     }
                     cp_async_commit();
-                    if (f > 0) {
-                        cp_async_wait<1>(); // this thread's copies of the previous stage have landed
+                    if (f >= kLag) {
+                        cp_async_wait<kLag>(); // this thread's copies of stage f - kLag have landed
                         fence_proxy_async_smem();
-                        mbar_arrive(ring.full_bar(f - 1));
+                        mbar_arrive(ring.full_bar(f - kLag));
                     }
                 } else {
-                    constexpr int kBatch = 8;
+                    // Each batch keeps kBatch chunk loads per thread in flight;
+                    // the batches tile the stage exactly (no chunk index past it).
+                    constexpr int kBatch = 32 / kCopyWarps;
+                    static_assert(kBatch >= 1 && kStageChunks % (kBatch * kCopyThreads) == 0,
+                                  "batches tile the stage exactly");
                     for (int q0 = ptid; q0 < kStageChunks; q0 += kBatch * kCopyThreads) {
                         uint4 v[kBatch];
                         uint32_t off[kBatch];
@@ -301,9 +331,10 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
         }
         if constexpr (Fill == GEMM_FILL_CPASYNC) {
             cp_async_wait<0>();
-            if (ok && f > 0) {
+            if (ok) {
                 fence_proxy_async_smem();
-                mbar_arrive(ring.full_bar(f - 1));
+                for (int g = f - kLag > 0 ? f - kLag : 0; g < f; ++g)
+                    mbar_arrive(ring.full_bar(g));
             }
         }
     } else if (warp == R::kMmaWarp) {
