@@ -22,17 +22,17 @@
 // The fills, as in the FP32 family ("Day 74: Async copies and pipelines", day
 // 80's goal of this pipeline feeding tensor cores):
 //   TMA       as above: one thread, one descriptor per box.
-//   cp.async  sixteen producer warps copy 16-byte chunks straight into the
-//             swizzled stage with cp.async (interior stages without guards),
-//             keep S-1 stages in flight per thread (wait_group S-2), and mark
-//             a stage full once their own copies of it have landed.  One
-//             thread cannot issue 3072 copies per stage fast enough, so the
-//             copy issue is spread over 512 threads; measured on GB300 at
-//             8192^3, S = 4: 268 TFLOP/s with four warps and one stage in
-//             flight, 675 with eight warps, 834 with sixteen.
-//   sync      the same sixteen warps load chunks into registers and store
-//             them into the one and only stage; loads and MMAs strictly
-//             alternate.
+//   cp.async  eight producer warps copy 16-byte chunks straight into the
+//             swizzled stage with cp.async, keep S-1 stages in flight per
+//             thread (wait_group S-2), and mark a stage full once their own
+//             copies of it have landed.  In an interior tile each thread's
+//             chunks sit at the same stage offsets for every K block and
+//             their sources advance by a fixed step, so the addresses are
+//             computed once per tile and each copy is one unguarded
+//             instruction.
+//   sync      sixteen producer warps load chunks into registers (an interior
+//             tile's six per thread all at once) and store them into the one
+//             and only stage; loads and MMAs strictly alternate.
 // The cp.async and sync producers write the 128-byte-swizzled layout the TMA
 // would write (16-byte chunk index XOR row mod 8 within each 1024-byte atom)
 // through the generic proxy; each writer issues fence.proxy.async before its
@@ -70,12 +70,25 @@ constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 KiB
 constexpr uint32_t kTmemCols = 2 * BN;                     // two accumulators
 constexpr int kGroupM = 16;
 constexpr int kStageChunks = kStageBytes / 16;           // 3072 16-byte chunks per stage
-constexpr int kCopyWarps = 16;                            // cp.async / sync producer warps
-constexpr int kCopyThreads = kCopyWarps * 32;
+// Producer warps per fill: the TMA fill needs one elected thread; the
+// thread-issued fills spread a stage's 3072 chunks over many threads (GB300,
+// 8192^3, four stages: cp.async 833 TFLOP/s with sixteen warps recomputing
+// every address, 1390 with sixteen and 1420 with eight precomputing them;
+// the register path 236 with sixteen warps in batches of two loads, 438
+// with all six of a thread's loads in flight at once).
+constexpr int kCpAsyncCopyWarps = 8;
+constexpr int kSyncCopyWarps = 16;
+
+template <int Fill>
+constexpr int copy_warps()
+{
+    return Fill == GEMM_FILL_TMA ? 1 : Fill == GEMM_FILL_CPASYNC ? kCpAsyncCopyWarps : kSyncCopyWarps;
+}
 
 template <int Fill>
 struct Roles {
-    static constexpr int kProducerWarps = Fill == GEMM_FILL_TMA ? 1 : kCopyWarps;
+    static constexpr int kProducerWarps = copy_warps<Fill>();
+    static constexpr int kCopyThreads = kProducerWarps * 32;
     static constexpr int kMmaWarp = kProducerWarps;
     static constexpr int kEpiWarp0 = kMmaWarp + 1;        // four epilogue warps
     static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
@@ -251,9 +264,29 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
         constexpr int kLag = S >= 3 ? S - 2 : 1;
         int f = 0;
         bool ok = true;
+        constexpr int kCopyThreads = R::kCopyThreads;
+        constexpr int kChunksPerThread = kStageChunks / kCopyThreads;
+        static_assert(kStageChunks % kCopyThreads == 0, "whole chunks per thread");
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, tiles_m, tiles_n, mb, nb);
+            // An interior tile's chunks: the same shared-memory offsets in
+            // every stage, sources that advance by a fixed step per K block.
+            const bool tile_interior = (mb + 1) * BM <= p.M && (nb + 1) * BN <= p.N;
+            uint32_t c_off[kChunksPerThread];
+            const uint16_t *c_src[kChunksPerThread];
+            long long c_step[kChunksPerThread];
+            if (tile_interior) {
+#pragma unroll
+                for (int i = 0; i < kChunksPerThread; ++i) {
+                    int grow, gcol;
+                    bool is_a;
+                    stage_chunk(ptid + i * kCopyThreads, mb, nb, 0, grow, gcol, is_a, c_off[i]);
+                    c_src[i] = is_a ? p.A + static_cast<long long>(grow) * p.lda + gcol
+                                    : p.B + static_cast<long long>(grow) * p.ldb + gcol;
+                    c_step[i] = is_a ? static_cast<long long>(BK) : static_cast<long long>(BK) * p.ldb;
+                }
+            }
             for (int kb = 0; kb < k_blocks; ++kb, ++f) {
                 const bool free = ring.producer_acquire(f, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, free)) {
@@ -264,18 +297,13 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                 }
                 const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
                 if constexpr (Fill == GEMM_FILL_CPASYNC) {
-                    const bool interior = (mb + 1) * BM <= p.M && (nb + 1) * BN <= p.N && (kb + 1) * BK <= p.K;
-                    if (interior) {
+                    if (tile_interior && (kb + 1) * BK <= p.K) {
                         // Every chunk is a whole in-range 16-byte copy (the
                         // planner requires 16-byte row pitches).
-                        for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
-                            int grow, gcol;
-                            bool is_a;
-                            uint32_t off;
-                            stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
-                            const uint16_t *src = is_a ? p.A + static_cast<long long>(grow) * p.lda + gcol
-                                                       : p.B + static_cast<long long>(grow) * p.ldb + gcol;
-                            cp_async_cg16_full(dst + off, src);
+#pragma unroll
+                        for (int i = 0; i < kChunksPerThread; ++i) {
+                            cp_async_cg16_full(dst + c_off[i], c_src[i]);
+                            c_src[i] += c_step[i];
                         }
                     } else {
                         for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
@@ -301,10 +329,25 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                         fence_proxy_async_smem();
                         mbar_arrive(ring.full_bar(f - kLag));
                     }
+                } else if (tile_interior && (kb + 1) * BK <= p.K) {
+                    // Interior: every chunk of this thread loaded at once, then stored.
+                    uint4 v[kChunksPerThread];
+#pragma unroll
+                    for (int i = 0; i < kChunksPerThread; ++i) {
+                        v[i] = *reinterpret_cast<const uint4 *>(c_src[i]);
+                        c_src[i] += c_step[i];
+                    }
+#pragma unroll
+                    for (int i = 0; i < kChunksPerThread; ++i)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst + c_off[i]), "r"(v[i].x),
+                                     "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    mbar_arrive(ring.full_bar(f));
                 } else {
                     // Each batch keeps kBatch chunk loads per thread in flight;
                     // the batches tile the stage exactly (no chunk index past it).
-                    constexpr int kBatch = 32 / kCopyWarps;
+                    constexpr int kBatch = 32 / R::kProducerWarps;
                     static_assert(kBatch >= 1 && kStageChunks % (kBatch * kCopyThreads) == 0,
                                   "batches tile the stage exactly");
                     for (int q0 = ptid; q0 < kStageChunks; q0 += kBatch * kCopyThreads) {
@@ -479,7 +522,9 @@ static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
 
 int bf16_threads(int fill)
 {
-    return fill == GEMM_FILL_TMA ? bf16::Roles<GEMM_FILL_TMA>::kThreads : bf16::Roles<GEMM_FILL_CPASYNC>::kThreads;
+    if (fill == GEMM_FILL_TMA)
+        return bf16::Roles<GEMM_FILL_TMA>::kThreads;
+    return fill == GEMM_FILL_CPASYNC ? bf16::Roles<GEMM_FILL_CPASYNC>::kThreads : bf16::Roles<GEMM_FILL_SYNC>::kThreads;
 }
 
 int launch_bf16(const Bf16Args &a, int fill, cudaStream_t s)

@@ -156,10 +156,10 @@ int gemm_f32_plan(int M, int N, int K,
  * while the tensor cores work on the current one).
  *
  *   fill_mode   GEMM_FILL_TMA (one thread issues 2-D tensor copies),
- *               GEMM_FILL_CPASYNC (sixteen producer warps copy 16-byte
+ *               GEMM_FILL_CPASYNC (eight producer warps copy 16-byte
  *               chunks with cp.async into the same swizzled stages), or
- *               GEMM_FILL_SYNC (the register path: producers load and
- *               store, one stage, loads and MMAs alternate).
+ *               GEMM_FILL_SYNC (the register path: sixteen producer warps
+ *               load and store, one stage, loads and MMAs alternate).
  *               GEMM_FILL_CPASYNC_MBAR returns GEMM_ERR_UNSUPPORTED.
  *   stages      TMA / cp.async: 2..4 (4 x 48 KiB fills shared memory), or
  *               0 for the default of 4.  sync: 0 or 1.

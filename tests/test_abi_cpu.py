@@ -149,7 +149,7 @@ def test_bf16_plan(lib):
     assert d["stages"] == 1 and d["threads"] == 672 and d["a_copy_bytes"] == 16
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 2, ctypes.byref(p)) == 1
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 1, 0, ctypes.byref(p)) == 0
-    assert p.as_dict()["stages"] == 4 and p.as_dict()["threads"] == 672
+    assert p.as_dict()["stages"] == 4 and p.as_dict()["threads"] == 416
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 3, 0, ctypes.byref(p)) == 3
     assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
     assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
