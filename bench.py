@@ -245,7 +245,7 @@ def profiled_traffic(kernel_key: str):
     sha, traffic = None, None
     with open(path) as f:
         for line in f:
-            line = line.strip().strip("`").strip("- ")
+            line = line.strip().strip("-` ")
             if line.startswith("source_sha:"):
                 sha = line.split(":", 1)[1].strip()
             if line.startswith(f"traffic_bytes_per_launch[{kernel_key}]:"):

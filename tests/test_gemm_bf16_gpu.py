@@ -52,6 +52,35 @@ def test_small_ragged_normal(fill, stages, M, N, K):
         np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+_WALK_CACHE = {}
+
+
+def _walk_case(M, N, K):
+    """Operands and oracle for a shape with more 128 x 256 tiles than SMs (so
+    persistent CTAs walk several tiles), cached across fills."""
+    key = (M, N, K)
+    if key not in _WALK_CACHE:
+        A, B = bf16_operands("normal", M, N, K, 70 + K)
+        want = oracle.gemm_bf16_f64(A, B, M, N, K)
+        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma")
+        _WALK_CACHE[key] = (A, B, want, ref, _abs_products(A, B, M, N, K))
+    return _WALK_CACHE[key]
+
+
+@pytest.mark.parametrize("fill,stages", BF16_FILLS)
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 192), (2000, 2600, 200)])
+def test_persistent_walk_interior_and_edge_tiles(fill, stages, M, N, K):
+    """160 / 176 tiles on at most 152 persistent CTAs.  The first shape has
+    only interior tiles and whole K blocks (the thread-issued fills' per-tile
+    address path throughout); the second mixes interior and edge tiles and
+    ends every tile with an 8-deep K tail (guarded path for edge tiles and for
+    the last K block)."""
+    A, B, want, ref, absprod = _walk_case(M, N, K)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+    _check(got, want, absprod, K, f"bf16 {fill} S{stages} {M}x{N}x{K}")
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("fill,stages", [("tma", 4), ("cpasync", 3), ("sync", 1)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 500), (513, 257, 1000)])
 def test_smallint_exact(fill, stages, M, N, K):

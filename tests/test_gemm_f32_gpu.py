@@ -265,16 +265,6 @@ def test_non_default_stream():
     assert_bitwise_equal(C.cpu().numpy(), oracle.gemm_fmaf_chain(A, B, M, N, K), "side stream")
 
 
-def test_host_row_chunks_cover_rows_once():
-    import async_copy_pipelined_gb300 as pg
-    for M in (1, 127, 1023, 1024, 2048, 2500, 4096, 9000):
-        ch = pg.host_row_chunks(M)
-        assert ch[0][0] == 0 and ch[-1][1] == M
-        assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))
-        assert all((r1 - r0) % 128 == 0 for r0, r1 in ch[:-1])
-        assert len(ch) <= pg.HOST_CHUNKS_MAX
-
-
 @pytest.mark.parametrize("fill", ["sync", "tma"])
 def test_host_tensors_chunked_match_device_path(fill):
     """A host call split into more row chunks than it has streams (so every

@@ -1,0 +1,59 @@
+"""Host-side logic that needs no GPU: the host path's row chunking, the
+bench's roofline peak arithmetic, its workload descriptions and the reader
+of the committed DRAM-traffic summary."""
+import pytest
+
+import async_copy_pipelined_gb300 as pg
+import bench
+from async_copy_pipelined_gb300 import inputs
+
+
+@pytest.mark.parametrize("M", [1, 127, 128, 511, 512, 1023, 1024, 2048, 2500, 3300, 4096, 9000, 65536])
+def test_host_row_chunks_cover_rows_once(M):
+    ch = pg.host_row_chunks(M)
+    assert ch[0][0] == 0 and ch[-1][1] == M
+    assert all(a[1] == b[0] and a[0] < a[1] for a, b in zip(ch, ch[1:]))
+    assert all((r1 - r0) % 128 == 0 for r0, r1 in ch[:-1])  # whole 128-row tiles but the last
+    assert len(ch) <= pg.HOST_CHUNKS_MAX
+    if M >= 2 * pg.HOST_CHUNK_MIN_ROWS:
+        assert len(ch) >= 2 and all(r1 - r0 >= pg.HOST_CHUNK_MIN_ROWS for r0, r1 in ch[:-1])
+
+
+def test_fp32_peak_is_sms_times_lanes_times_clock():
+    # 152 SMs x 128 FP32 lanes x 2 flops per FMA x 2070 MHz
+    assert bench.fp32_peak_tflops(152, 2070.0) == pytest.approx(80.54784)
+    assert bench.fp32_peak_tflops(76, 1000.0) == pytest.approx(76 * 128 * 2 * 1e9 / 1e12)
+
+
+@pytest.mark.parametrize("name", sorted(inputs.WORKLOADS))
+def test_workload_config_names_sizes(name):
+    w = inputs.WORKLOADS[name]
+    cfg = bench.workload_config(name, w, {"fill": "tma"})
+    assert (cfg["M"], cfg["N"], cfg["K"], cfg["lda"]) == (w["M"], w["N"], w["K"], w["lda"])
+    assert cfg["fill"] == "tma" and "flushed" in cfg["l2"] and str(w["seed"]) in cfg["workload"]
+
+
+def test_profiled_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.md").write_text(
+        "# traffic\n\n- source_sha: 0123abcd\n"
+        "- traffic_bytes_per_launch[f32_4096:tma/S4/T128]: 329889792\n"
+        "- `traffic_bytes_per_launch[bf16_8192:tma/S4/T0]: 1242865152`\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "0123abcd")
+    assert bench.profiled_traffic("f32_4096:tma/S4/T128") == 329889792
+    assert bench.profiled_traffic("bf16_8192:tma/S4/T0") == 1242865152  # key holds a colon
+    assert bench.profiled_traffic("f32_4096:cpasync/S4/T128") is None
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "ffffffff")  # sources changed since
+    assert bench.profiled_traffic("f32_4096:tma/S4/T128") is None
+
+
+def test_kernel_sources_sha_covers_every_source(tmp_path, monkeypatch):
+    csrc = tmp_path / "async_copy_pipelined_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cu").write_text("x")
+    (csrc / "b.cuh").write_text("y")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h1 = bench.kernel_sources_sha()
+    (csrc / "b.cuh").write_text("z")
+    assert bench.kernel_sources_sha() != h1
