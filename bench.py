@@ -519,8 +519,8 @@ def run_ours(args, dist: Dist):
             Ctd = torch.empty((wt["M"], wt["N"]), dtype=torch.float32, device=dev)
             ft = 2.0 * wt["M"] * wt["N"] * wt["K"]
             tall = {}
-            for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("tma", 2), ("tma", 4), ("cpasync_mbar", 2),
-                         ("cpasync_mbar", 4)):
+            for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("cpasync", 6), ("tma", 2), ("tma", 4),
+                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4), ("cpasync_mbar", 6)):
                 c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
                 mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches

@@ -211,7 +211,7 @@ def test_workload_tallk_one_warp_all_fills():
     want32 = oracle.gemm_fmaf_chain(A, B, M, N, K)
     want64 = oracle.gemm_f64(A, B, M, N, K)
     for fill, stages in [("sync", 1), ("cpasync", 2), ("cpasync", 4), ("cpasync", 6), ("tma", 2), ("tma", 4),
-                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4)]:
+                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4), ("cpasync_mbar", 6)]:
         got, _ = run_f32(A, B, M, N, K, fill, stages, 32)
         assert_bitwise_equal(got, want32, f"tall-K {fill}/S{stages}")
     assert np.max(np.abs(got - want64)) <= 1e-5 * K
