@@ -340,7 +340,7 @@ const char *gemm_status_string(int status)
     case GEMM_OK: return "GEMM_OK";
     case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid size, leading dimension, pointer, fill, stages or tile";
     case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: base or row pitch not aligned as the fill requires";
-    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: request not implemented by this build";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: the library does not implement this request";
     case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: current device is not compute capability 10.3 (sm_103a)";
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime or driver call failed";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel's bounded wait expired";
