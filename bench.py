@@ -604,10 +604,14 @@ def run_ours(args, dist: Dist):
                                             block_tile=leg["tile"])
         e_steps = max(3, min(args.steps, 20))
         wt = WallTimer()
-        e_total, _ = timed_loop(_NoDist(), e_steps, 3, host_call, lambda: None, wt, torch.cuda.synchronize)
-        e2e = {"value": flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(Ah.element_size() * M * K + Bh.element_size() * K * N),
-               "d2h_bytes_per_step": int(4 * M * N), "ms_per_step": e_total / e_steps}
+        # With several ranks: barrier + sync around exactly e_steps steps and
+        # the max over ranks, like the device-timed leg; whole-job throughput
+        # and bytes summed over the ranks.
+        e_total, _ = timed_loop(dist if dist.world > 1 else _NoDist(), e_steps, 3, host_call, lambda: None, wt,
+                                torch.cuda.synchronize)
+        e2e = {"value": dist.world * flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": dist.world * int(Ah.element_size() * M * K + Bh.element_size() * K * N),
+               "d2h_bytes_per_step": dist.world * int(4 * M * N), "ms_per_step": e_total / e_steps}
         # One GEMM launch per row chunk of the host path, every step.
         launches_e2e = e_steps * len(pg.host_row_chunks(M))
 
