@@ -128,6 +128,20 @@ def _matrix_args(x, name):
     return rows, cols, max(ld, 1), x.data_ptr()
 
 
+def _operand_device(A, B, C, stream):
+    """The one device A, B and C (if given) all live on; the kernels read and
+    write them through raw pointers, so mixed host/device operands or
+    operands on two GPUs are refused rather than launched."""
+    for name, t in (("B", B), ("C", C)):
+        if t is not None and t.device != A.device:
+            raise ValueError(f"A is on {A.device} but {name} is on {t.device}: "
+                             "all operands must be on one device (or all on the host)")
+    dev = A.device
+    if dev.type == "cuda" and stream is not None and getattr(stream, "device", dev) != dev:
+        raise ValueError(f"stream belongs to {stream.device}, operands to {dev}")
+    return dev
+
+
 def _check(status: int, what: str):
     if status != GEMM_OK:
         raise GemmError(status, what)
@@ -229,6 +243,7 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     once C is on the host.
     """
     import torch
+    dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
         if block_tile == 0:
             # The tile the whole problem would get, not what one row chunk
@@ -247,12 +262,13 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     if K2 != K:
         raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
     if C is None:
-        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
-    st = lib().gemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_tile,
-                        _stream_handle(stream))
+    with torch.cuda.device(dev):
+        st = lib().gemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_tile,
+                            _stream_handle(stream))
     _check(st, "gemm_f32")
     return C
 
@@ -263,6 +279,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
     fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
     the MMAs read; all three give the same bits."""
     import torch
+    dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
         return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=s),
                                A, B, C, torch.float32)
@@ -273,11 +290,13 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
     if K2 != K:
         raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
     if C is None:
-        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
-    st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, _stream_handle(stream))
+    with torch.cuda.device(dev):
+        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages,
+                             _stream_handle(stream))
     _check(st, "gemm_bf16")
     return C
 

@@ -70,3 +70,26 @@ def test_refusals_enqueue_nothing():
     torch.cuda.synchronize()
     assert torch.all(C == 9.0), "a refused call wrote C"
     assert pg.device_status()[0] == 0
+
+
+def test_mixed_host_and_device_operands_are_refused():
+    """The kernels take raw pointers, so a host tensor next to device ones
+    would be read as device memory: the binding refuses the call before any
+    launch, for both GEMMs and for an output on the wrong side."""
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    Ad = torch.ones((64, 32), device="cuda")
+    Bd = torch.ones((32, 48), device="cuda")
+    Ah, Bh = Ad.cpu(), Bd.cpu()
+    with pytest.raises(ValueError, match="one device"):
+        pg.gemm_f32(Ad, Bh)
+    with pytest.raises(ValueError, match="one device"):
+        pg.gemm_f32(Ad, Bd, torch.empty((64, 48)))
+    with pytest.raises(ValueError, match="one device"):
+        pg.gemm_f32(Ah, Bd)  # host call with a device B
+    with pytest.raises(ValueError, match="one device"):
+        pg.gemm_bf16(Ad.bfloat16(), Bh.bfloat16())
+    torch.cuda.synchronize()
+    assert pg.device_status()[0] == 0
+    C = pg.gemm_f32(Ad, Bd)  # the context still works
+    assert torch.equal(C, torch.full((64, 48), 32.0, device="cuda"))
