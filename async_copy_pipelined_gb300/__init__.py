@@ -142,6 +142,25 @@ def _operand_device(A, B, C, stream):
     return dev
 
 
+def _byte_range(x):
+    """[first, last) bytes a row-major 2-D tensor view spans."""
+    rows, cols = x.shape
+    if rows == 0 or cols == 0:
+        return (0, 0)
+    first = x.data_ptr()
+    return first, first + ((rows - 1) * x.stride(0) + cols) * x.element_size()
+
+
+def _refuse_aliased_output(C, A, B):
+    """C is written while other blocks still read A and B: an output that
+    shares bytes with an input would give wrong results, so it is refused."""
+    c0, c1 = _byte_range(C)
+    for name, t in (("A", A), ("B", B)):
+        t0, t1 = _byte_range(t)
+        if c0 < t1 and t0 < c1:
+            raise ValueError(f"C overlaps {name} in memory; the output must not alias an input")
+
+
 def _check(status: int, what: str):
     if status != GEMM_OK:
         raise GemmError(status, what)
@@ -245,6 +264,8 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     import torch
     dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
+        if C is not None:
+            _refuse_aliased_output(C, A, B)
         if block_tile == 0:
             # The tile the whole problem would get, not what one row chunk
             # alone would get.
@@ -266,6 +287,7 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
+    _refuse_aliased_output(C, A, B)
     with torch.cuda.device(dev):
         st = lib().gemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_tile,
                             _stream_handle(stream))
@@ -281,6 +303,8 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
     import torch
     dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
+        if C is not None:
+            _refuse_aliased_output(C, A, B)
         return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=s),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
@@ -294,6 +318,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
+    _refuse_aliased_output(C, A, B)
     with torch.cuda.device(dev):
         st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages,
                              _stream_handle(stream))

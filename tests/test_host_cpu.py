@@ -57,3 +57,30 @@ def test_kernel_sources_sha_covers_every_source(tmp_path, monkeypatch):
     h1 = bench.kernel_sources_sha()
     (csrc / "b.cuh").write_text("z")
     assert bench.kernel_sources_sha() != h1
+
+
+def test_aliased_output_is_refused():
+    """Byte-range overlap of C with A or B (views of one buffer) is refused;
+    disjoint views of the same buffer are accepted."""
+    import torch
+    buf = torch.zeros(4096)
+    A = buf[:1024].view(32, 32)
+    B = buf[1024:2048].view(32, 32)
+    pg._refuse_aliased_output(buf[2048:3072].view(32, 32), A, B)  # disjoint: no error
+    with pytest.raises(ValueError, match="overlaps A"):
+        pg._refuse_aliased_output(A, A, B)
+    with pytest.raises(ValueError, match="overlaps B"):
+        pg._refuse_aliased_output(buf[1500:2524].view(32, 32), A, B)
+    # A padded view (ld 40 > 32 columns) spans through its last row only.
+    Ap = buf[:40 * 31 + 32].as_strided((32, 32), (40, 1))
+    pg._refuse_aliased_output(buf[40 * 31 + 32: 40 * 31 + 32 + 1024].view(32, 32), Ap, B[:1, :1])
+
+
+def test_host_call_refuses_aliased_output_before_touching_a_gpu():
+    import torch
+    A = torch.zeros((64, 64))
+    B = torch.zeros((64, 64))
+    with pytest.raises(ValueError, match="overlaps A"):
+        pg.gemm_f32(A, B, A)
+    with pytest.raises(ValueError, match="one device"):
+        pg.gemm_f32(A, B.to("meta"))
