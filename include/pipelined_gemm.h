@@ -41,7 +41,10 @@
  *
  * Ownership: every pointer is a device pointer owned by the caller; the
  * library keeps no reference after the call returns.  The entry points
- * allocate no memory.
+ * allocate no memory.  The library cannot check two preconditions, and
+ * breaking either is undefined behaviour: A, B and C are memory of the
+ * current device (cudaSetDevice), and C shares no byte with A or B (other
+ * blocks still read A and B while C tiles are written).
  *
  * Asynchrony: gemm_f32 / gemm_bf16 enqueue one kernel on `stream` (a
  * cudaStream_t; NULL means the legacy default stream) and return without
@@ -73,7 +76,7 @@ typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1, /* bad size, leading dimension, pointer, fill, stages or tile   */
     GEMM_ERR_MISALIGNED = 2,  /* TMA needs 16-byte aligned bases and row pitches              */
-    GEMM_ERR_UNSUPPORTED = 3, /* valid request this build does not implement                  */
+    GEMM_ERR_UNSUPPORTED = 3, /* valid request the library does not implement                 */
     GEMM_ERR_ARCH = 4,        /* current device is not compute capability 10.3 (sm_103a)      */
     GEMM_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed (launch, attribute, ...)   */
     GEMM_ERR_TIMEOUT = 6      /* a kernel's bounded wait expired (read via gemm_device_status) */
