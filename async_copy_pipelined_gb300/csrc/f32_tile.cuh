@@ -182,11 +182,23 @@ struct FragPipe {
     __device__ __forceinline__ const float *run(const float *__restrict__ sA, const float *__restrict__ sB, int tr,
                                                 int tc, Accum<T> &acc, Release &&release, Next &&next)
     {
+        return run_mid(sA, sB, tr, tc, acc, release, next, []() {});
+    }
+
+    // As run(), and calls `mid` once, halfway through the slice (before the
+    // FMAs of k = BK/2): a fill can issue its next copies there.
+    template <class Release, class Next, class Mid>
+    __device__ __forceinline__ const float *run_mid(const float *__restrict__ sA, const float *__restrict__ sB,
+                                                    int tr, int tc, Accum<T> &acc, Release &&release, Next &&next,
+                                                    Mid &&mid)
+    {
         const float *nA = nullptr;
 #pragma unroll
         for (int k = 0; k < T::BK; ++k) {
             const int ab = (k / 4) & 1;
             const int bb = k & 1;
+            if (k == T::BK / 2)
+                mid();
             if ((k & 3) == 0 && k + 4 < T::BK)
                 load_a_frag<T>(sA, tr, k / 4 + 1, a[ab ^ 1]);
             if (k + 1 < T::BK)
