@@ -627,6 +627,13 @@ def run_ours(args, dist: Dist):
                                f"({peaks['_source']} max SM clock)"}
         if clocks.get("sm_mhz"):
             roof["frac_at_observed_clock"] = achieved / fp32_peak_tflops(num_sms, clocks["sm_mhz"])
+    # Diagnostic, not the bound: the DRAM rate the profiled traffic implies
+    # at this launch's mean duration, against the measured copy bandwidth.
+    if roof.get("traffic"):
+        hbm = float(peaks.get("hbm_gbs") or 0.0)
+        dram_gbs = roof["traffic"] / (local_mean / 1e3) / 1e9
+        roof["dram_gbs"] = dram_gbs
+        roof["dram_frac_of_hbm"] = dram_gbs / hbm if hbm else None
 
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
