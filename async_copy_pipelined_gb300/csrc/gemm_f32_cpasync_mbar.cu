@@ -16,9 +16,11 @@
 //   consumer_release  one arrive per warp on empty[s]
 //
 // No CTA-wide barrier sits in the main loop; a warp only waits for the
-// slowest warp of the slice whose stage it is about to refill (one slice of
-// slack).  Zero fill, chunk mapping and the inner product are those of the
-// cp.async fill, so results are bit-identical to the other fills.  Waits are
+// slowest warp of the slice whose stage it is about to refill.  From three
+// stages on, that refill is issued halfway through a slice into the stage
+// released two slices earlier, so the wait is normally already satisfied.
+// Zero fill, chunk mapping and the inner product are those of the cp.async
+// fill, so results are bit-identical to the other fills.  Waits are
 // bounded; on expiry the warp records GEMM_ERR_TIMEOUT and stops, and every
 // thread drains its own copies (cp.async.wait_all) before exit.
 #include "f32_tile.cuh"

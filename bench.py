@@ -222,16 +222,46 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- profiles
+def _code_only(src: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed
+    (string and character literals are kept as they are)."""
+    out, i, n, quote = [], 0, len(src), None
+    while i < n:
+        c = src[i]
+        if quote is None:
+            if src.startswith("//", i):
+                j = src.find("\n", i)
+                i = n if j < 0 else j
+                continue
+            if src.startswith("/*", i):
+                j = src.find("*/", i + 2)
+                i = n if j < 0 else j + 2
+                out.append(" ")
+                continue
+            if c in "\"'":
+                quote = c
+        elif c == "\\" and i + 1 < n:
+            out.append(src[i:i + 2])
+            i += 2
+            continue
+        elif c == quote:
+            quote = None
+        out.append(c)
+        i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sources_sha() -> str:
-    """Hash of the CUDA sources; a traffic figure captured for other sources is stale."""
+    """Hash of the CUDA sources' code (comments and whitespace ignored); a
+    traffic figure captured for other code is stale."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "async_copy_pipelined_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

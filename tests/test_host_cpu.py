@@ -84,3 +84,18 @@ def test_host_call_refuses_aliased_output_before_touching_a_gpu():
         pg.gemm_f32(A, B, A)
     with pytest.raises(ValueError, match="one device"):
         pg.gemm_f32(A, B.to("meta"))
+
+
+def test_kernel_sources_sha_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    csrc = tmp_path / "async_copy_pipelined_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    f = csrc / "k.cu"
+    f.write_text('// header\nint a = 1; /* block */ const char *s = "x // y";\n')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h1 = bench.kernel_sources_sha()
+    f.write_text('// another header\n\nint a = 1;   /* other */ const char *s = "x // y";\n')
+    assert bench.kernel_sources_sha() == h1  # comments and whitespace only
+    f.write_text('// header\nint a = 2; /* block */ const char *s = "x // y";\n')
+    assert bench.kernel_sources_sha() != h1  # code
+    f.write_text('// header\nint a = 1; /* block */ const char *s = "x // z";\n')
+    assert bench.kernel_sources_sha() != h1  # text inside a string literal is code
