@@ -24,9 +24,14 @@ constexpr int kDefaultStagesCpAsync = 3;
 constexpr int kDefaultStagesTma = 4;
 constexpr int kDefaultStagesBf16 = 4;
 constexpr int kMaxStagesBf16 = 4;
-// Two resident 128x128 CTAs per SM on a 152-SM GB300: below this many
-// 128x128 tiles the 64x64 tile gives the better-filled grid.
-constexpr long long kLargeTileMinTiles = 304;
+// block_tile = 0 picks the 128x128 tile from this many 128x128 tiles on (a
+// little under one wave at one CTA per SM on a 152-SM GB300); below it the
+// 64x64 tile, three CTAs per SM, fills the GPU better.  Measured on GB300
+// (TMA, four stages, TFLOP/s for the 64 / 128 tile): 64 tiles (1024^3)
+// 37.0 / 23.9, 100 tiles (1280^3) 40.7 / 38.1, 128 tiles (512 x 4096 x
+// 4096 and two other shapes) 41.8 / 51.1, 144 tiles (1536^3) 43.8 / 55.4;
+// the cp.async and register fills cross over at the same point.
+constexpr long long kLargeTileMinTiles = 120;
 
 __device__ unsigned int g_status_word;
 
