@@ -77,7 +77,7 @@ def test_plan_defaults_and_shapes(lib):
     assert st == 0 and p["block_m"] == 128 and p["stages"] == 4 and p["threads"] == 288
     assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (32, 32, 256)
     st, p = _plan(1024, 1024, 1024, fill=1)
-    assert st == 0 and p["block_m"] == 64 and p["threads"] == 256 and p["stages"] == 3
+    assert st == 0 and p["block_m"] == 64 and p["threads"] == 256 and p["stages"] == 4
     assert (p["grid_x"], p["grid_y"]) == (16, 16)
     st, p = _plan(4096, 4096, 4096, fill=3, stages=4)
     assert st == 0 and p["threads"] == 256 and p["a_copy_bytes"] == 16
@@ -93,7 +93,7 @@ def test_plan_defaults_and_shapes(lib):
     assert st == 0 and p["threads"] == 64 and (p["thread_m"], p["thread_n"]) == (8, 4)
     assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (1, 1, 4096)
     st, p = _plan(32, 32, 65536, fill=1, tile=32)
-    assert st == 0 and p["threads"] == 32 and p["smem_bytes"] == 3 * 4096
+    assert st == 0 and p["threads"] == 32 and p["smem_bytes"] == 4 * 4096
     # The lesson's shared-memory arithmetic: one 64x64x16 stage is 8 KiB.
     for s in (2, 3, 4, 5, 6):
         st, p = _plan(512, 512, 512, fill=1, stages=s, tile=64)
@@ -154,6 +154,7 @@ def test_bf16_plan(lib):
     assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
     assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, ctypes.byref(p)) == 1
+
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
