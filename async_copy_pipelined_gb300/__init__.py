@@ -67,9 +67,9 @@ def _bind(l):
     l.gemm_f32.restype = I
     l.gemm_f32_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, ctypes.POINTER(GemmPlan)]
     l.gemm_f32_plan.restype = I
-    l.gemm_bf16.argtypes = [I, I, I, P, I, P, I, P, I, I, I, P]
+    l.gemm_bf16.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]
     l.gemm_bf16.restype = I
-    l.gemm_bf16_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, ctypes.POINTER(GemmPlan)]
+    l.gemm_bf16_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, ctypes.POINTER(GemmPlan)]
     l.gemm_bf16_plan.restype = I
     l.gemm_status_string.argtypes = [I]
     l.gemm_status_string.restype = ctypes.c_char_p
@@ -176,11 +176,11 @@ def plan_f32(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_
     return p.as_dict()
 
 
-def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, a_ptr=256, b_ptr=256,
+def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_m=0, a_ptr=256, b_ptr=256,
               c_ptr=256) -> dict:
     p = GemmPlan()
     st = lib().gemm_bf16_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
-                              _fill_code(fill), stages, ctypes.byref(p))
+                              _fill_code(fill), stages, block_m, ctypes.byref(p))
     _check(st, "gemm_bf16_plan")
     return p.as_dict()
 
@@ -295,17 +295,28 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     return C
 
 
-def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
+def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
     """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores.
 
     fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
-    the MMAs read; all three give the same bits."""
+    the MMAs read; block_m: 128 or 256 rows per CTA tile, 0 to let the
+    library choose.  Every fill and tile gives the same bits."""
     import torch
     dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
         if C is not None:
             _refuse_aliased_output(C, A, B)
-        return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, stream=s),
+        if block_m == 0:
+            # The tile the whole problem would get, not what one row chunk
+            # alone would get.
+            M, K, N = A.shape[0], A.shape[1], B.shape[1]
+            try:
+                block_m = plan_bf16(M, N, K, lda=(K + 7) // 8 * 8, ldb=(N + 7) // 8 * 8, fill=fill,
+                                    stages=stages)["block_m"]
+            except (RuntimeError, ValueError):
+                pass  # the chunk calls report the error
+        return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, block_m=block_m,
+                                                         stream=s),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")
@@ -320,7 +331,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, stream=None):
         raise ValueError("C must be a float32 M x N tensor")
     _refuse_aliased_output(C, A, B)
     with torch.cuda.device(dev):
-        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages,
+        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_m,
                              _stream_handle(stream))
     _check(st, "gemm_bf16")
     return C

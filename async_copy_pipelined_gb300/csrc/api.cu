@@ -27,8 +27,12 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull; // 2 s
 // 1923 us at 4).  At one CTA per SM the fourth 32 KiB stage costs no
 // occupancy; the 64x64 tile's three CTAs per SM take 96 KiB.
 constexpr int kDefaultStagesF32 = 4;
-constexpr int kDefaultStagesBf16 = 4;
-constexpr int kMaxStagesBf16 = 4;
+// BF16 ring depth: four 48 KiB stages for the 128-row tile, three 64 KiB
+// stages for the 256-row tile (four of those do not fit in 227 KiB).
+constexpr int kDefaultStagesBf16Tile128 = 4;
+constexpr int kDefaultStagesBf16Tile256 = 3;
+// block_m = 0 picks the 256-row BF16 tile from this many 256 x 256 tiles on.
+constexpr long long kBf16TallTileMinTiles = 120;
 // block_tile = 0 picks the 128x128 tile from this many 128x128 tiles on (a
 // little under one wave at one CTA per SM on a 152-SM GB300); below it the
 // 64x64 tile, three CTAs per SM, fills the GPU better.  Measured on GB300
@@ -151,10 +155,11 @@ int f32_smem_bytes(int tile, int fill, int stages)
 // SM's 228 KB.
 constexpr int kBf16ExclusiveSmemBytes = 116 * 1024;
 
-int bf16_smem_bytes(int stages)
+int bf16_smem_bytes(int stages, int block_m)
 {
-    const int stage_bytes = (kBf16BlockM * kBf16BlockK + kBf16BlockK * kBf16BlockN) * 2;
-    const int need = stages * stage_bytes + 1024 /* barriers, TMEM slot */ + 1024 /* alignment slack */;
+    const int stage_bytes = (block_m * kBf16BlockK + kBf16BlockK * kBf16BlockN) * 2;
+    const int staging = (block_m / 128) * 4 * 4096; // one 32 x 32 FP32 box per epilogue warp
+    const int need = stages * stage_bytes + staging + 1024 /* barriers, TMEM slot */ + 1024 /* alignment slack */;
     return need > kBf16ExclusiveSmemBytes ? need : kBf16ExclusiveSmemBytes;
 }
 
@@ -247,12 +252,14 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
 }
 
 static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
-                     int fill, int stages, gemm_plan *plan, Bf16Args *args)
+                     int fill, int stages, int block_m, gemm_plan *plan, Bf16Args *args)
 {
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
     if (fill == GEMM_FILL_CPASYNC_MBAR)
         return GEMM_ERR_UNSUPPORTED;
+    if (block_m != 0 && block_m != 128 && block_m != 256)
+        return GEMM_ERR_INVALID_ARG;
     if (fill != GEMM_FILL_TMA && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_SYNC)
         return GEMM_ERR_INVALID_ARG;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
@@ -260,36 +267,42 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
     const bool work = M > 0 && N > 0;
     if (work && (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))))
         return GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_SYNC) {
-        // The register-path fill has one stage: loads and MMAs alternate.
-        if (stages != 0 && stages != 1)
-            return GEMM_ERR_INVALID_ARG;
-        stages = 1;
-    } else {
-        if (stages == 0)
-            stages = kDefaultStagesBf16;
-        if (stages < 2 || stages > kMaxStagesBf16)
-            return GEMM_ERR_INVALID_ARG;
+    if (fill == GEMM_FILL_SYNC && stages != 0 && stages != 1)
+        return GEMM_ERR_INVALID_ARG; // the register-path fill has one stage: loads and MMAs alternate
+    if (fill != GEMM_FILL_SYNC && stages != 0 && (stages < 2 || stages > kDefaultStagesBf16Tile128))
+        return GEMM_ERR_INVALID_ARG;
+    if (block_m == 0) {
+        // Four stages only fit the 128-row tile; otherwise the 256-row tile
+        // once there are enough of them to fill the GPU.
+        const long long tall_tiles =
+            static_cast<long long>((M + 255) / 256) * ((N + kBf16BlockN - 1) / kBf16BlockN);
+        block_m = (stages == 4 || tall_tiles < kBf16TallTileMinTiles) ? 128 : 256;
     }
+    if (fill == GEMM_FILL_SYNC)
+        stages = 1;
+    else if (stages == 0)
+        stages = block_m == 256 ? kDefaultStagesBf16Tile256 : kDefaultStagesBf16Tile128;
+    if (block_m == 256 && stages > kDefaultStagesBf16Tile256)
+        return GEMM_ERR_INVALID_ARG;
     if (!aligned4(C))
         return GEMM_ERR_MISALIGNED;
     if (work && K > 0 && (!aligned16(A) || !aligned16(B) || (lda % 8) != 0 || (ldb % 8) != 0))
         return GEMM_ERR_MISALIGNED;
-    const long long tiles_m = (M + kBf16BlockM - 1) / kBf16BlockM;
+    const long long tiles_m = (M + block_m - 1) / block_m;
     const long long tiles_n = (N + kBf16BlockN - 1) / kBf16BlockN;
     if (tiles_m * tiles_n > 0x7fffffffLL)
         return GEMM_ERR_INVALID_ARG;
     if (plan) {
         std::memset(plan, 0, sizeof *plan);
         plan->fill_mode = fill;
-        plan->block_m = kBf16BlockM;
+        plan->block_m = block_m;
         plan->block_n = kBf16BlockN;
         plan->block_k = kBf16BlockK;
-        plan->threads = bf16_threads(fill);
+        plan->threads = bf16_threads(fill, block_m);
         plan->stages = stages;
-        plan->a_copy_bytes = fill == GEMM_FILL_TMA ? kBf16BlockM * kBf16BlockK * 2 : 16;
+        plan->a_copy_bytes = fill == GEMM_FILL_TMA ? block_m * kBf16BlockK * 2 : 16;
         plan->b_copy_bytes = fill == GEMM_FILL_TMA ? kBf16BlockK * 64 * 2 : 16;
-        plan->smem_bytes = bf16_smem_bytes(stages);
+        plan->smem_bytes = bf16_smem_bytes(stages, block_m);
         plan->grid_x = static_cast<int>(tiles_m * tiles_n); // upper bound; capped at the SM count on launch
         plan->grid_y = 1;
         plan->k_slices = (K + kBf16BlockK - 1) / kBf16BlockK;
@@ -305,6 +318,8 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         args->C = C;
         args->ldc = ldc;
         args->stages = stages;
+        args->block_m = block_m;
+        args->c_tma = aligned16(C) && (ldc % 4) == 0 ? 1 : 0;
         args->status = nullptr;
         args->wait_limit_ns = kDefaultWaitLimitNs;
         args->num_sms = 0;
@@ -394,18 +409,18 @@ int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int l
 }
 
 int gemm_bf16_plan(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
-                   int fill_mode, int stages, gemm_plan *plan)
+                   int fill_mode, int stages, int block_m, gemm_plan *plan)
 {
     if (!plan)
         return GEMM_ERR_INVALID_ARG;
-    return plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, plan, nullptr);
+    return plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_m, plan, nullptr);
 }
 
 int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
-              int fill_mode, int stages, void *stream)
+              int fill_mode, int stages, int block_m, void *stream)
 {
     Bf16Args args;
-    int st = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, nullptr, &args);
+    int st = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_m, nullptr, &args);
     if (st != GEMM_OK)
         return st;
     int dev;

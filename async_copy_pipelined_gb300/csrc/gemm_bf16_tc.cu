@@ -3,21 +3,32 @@
 //
 // The pages' tensor-core loop ("异步拷贝与现代 Pipeline", section 6.1
 // "BF16 GEMM 的异步拷贝": prefetch the next K tile, commit, compute the current
-// tile on the tensor cores, wait, barrier) re-designed for sm_103a:
+// tile on the tensor cores, wait, barrier) re-designed for sm_103a.  A CTA
+// tile is MH x 128 rows by 256 columns (MH = 1 or 2):
 //
-//   warp 0      TMA producer: per 64-deep K block, one 128 x 64 box of A and
-//               four 64 x 64 boxes of B (128-byte swizzle) into ring stage
-//               f % S, announced on full[f % S].
-//   warp 1      allocates tensor memory (512 columns: two 128 x 256 FP32
-//               accumulators) and, from one thread, issues
-//               tcgen05.mma.cta_group::1.kind::f16 (M 128, N 256, K 16; four
-//               per K block); tcgen05.commit releases each ring stage to the
-//               producer once its MMAs have read it, and marks an
+//   warp 0      TMA producer: per 64-deep K block, one (MH x 128) x 64 box of
+//               A and four 64 x 64 boxes of B (128-byte swizzle) into ring
+//               stage f % S, announced on full[f % S].
+//   next warp   allocates all 512 columns of tensor memory and, from one
+//               thread, issues tcgen05.mma.cta_group::1.kind::f16 (M 128,
+//               N 256, K 16; four per K block for each 128-row half, the
+//               halves sharing each B slice); tcgen05.commit releases each
+//               ring stage once its MMAs have read it, and marks the
 //               accumulator full after a tile's last K block.
-//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (each warp
-//               its 32-lane quarter of tensor memory), FP32 stores to C, then
-//               hand the accumulator back.  With two accumulators the
-//               epilogue of tile i overlaps the MMAs of tile i+1.
+//   4 x MH warps  epilogue: tcgen05.ld of the finished accumulator (each warp
+//               a 32-lane quarter of tensor memory for one half), then TMA
+//               stores of 32 x 32 FP32 boxes through a swizzled per-warp
+//               staging buffer, then hand the accumulator back.
+//
+// Tensor memory holds two 128 x 256 FP32 accumulators.  The 128-row tile uses
+// them as a double buffer, so the epilogue of tile i overlaps the MMAs of
+// tile i+1.  The 256-row tile uses both for one tile: each B slice then feeds
+// two MMAs, so the shared-memory bytes written by the fill and read by the
+// tensor core per multiply-add drop by a third.  Shared-memory bandwidth,
+// which those writes and reads share, is what bounds the 128-row tile
+// (measured on GB300 at 8192^3: the MMAs alone, with no loads after the
+// first ring, run at 2140 TFLOP/s, the full kernel at 1667); the price is an
+// epilogue that no longer overlaps the next tile's MMAs.
 //
 // The fills, as in the FP32 family ("Day 74: Async copies and pipelines", day
 // 80's goal of this pipeline feeding tensor cores):
@@ -31,24 +42,31 @@
 //             computed once per tile and each copy is one unguarded
 //             instruction.
 //   sync      sixteen producer warps load chunks into registers (an interior
-//             tile's six per thread all at once) and store them into the one
-//             and only stage; loads and MMAs strictly alternate.
+//             tile's chunks of a thread all at once) and store them into the
+//             one and only stage; loads and MMAs strictly alternate.
 // The cp.async and sync producers write the 128-byte-swizzled layout the TMA
 // would write (16-byte chunk index XOR row mod 8 within each 1024-byte atom)
 // through the generic proxy; each writer issues fence.proxy.async before its
-// mbarrier arrive so the tensor core (async proxy) sees the data.
+// mbarrier arrive so the tensor core (async proxy) sees the data.  Every
+// fill and both tiles issue the same MMAs in the same K order for every
+// output element, so all of them give the same bits.
 //
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ... in
-// groups of 16 M-tiles so the tiles in flight share A and B rows in L2.
-// Ragged M, N, K: TMA zero-fills out-of-range box elements (zeros add nothing
-// to the products) and the epilogue guards its stores.
+// groups of 2048 rows of tiles so the tiles in flight share A and B rows in
+// L2.  Ragged M, N, K: TMA zero-fills out-of-range box elements (zeros add
+// nothing to the products), the TMA stores clip at the matrix edge, and the
+// plain-store epilogue (C not 16-byte aligned) guards each element.
 //
 // Layouts (PTX ISA shared-memory matrix descriptors, 128-byte swizzle):
-//   A stage  128 rows (m) x 128 bytes (64 k), K-major; 8-row groups 1024 B
-//            apart (SBO); the K step of 16 elements advances 32 bytes.
+//   A stage  MH x 128 rows (m) x 128 bytes (64 k), K-major; 8-row groups
+//            1024 B apart (SBO); the K step of 16 elements advances 32 bytes;
+//            half h starts 16 KiB in.
 //   B stage  four 64(n) x 64(k) boxes, each 64 rows (k) of 128 bytes (64 n):
 //            N-major ("MN-major"); 64-column atoms 8192 B apart (LBO), 8-row K
 //            groups 1024 B apart (SBO); the K step advances 16 rows = 2048 B.
+//   staging  per epilogue warp 32 rows x 128 bytes (32 FP32 columns), 16-byte
+//            chunk index XOR row mod 8, as the C tensor map's 128-byte
+//            swizzle expects.
 #include <cstring>
 
 #include "gemm_internal.h"
@@ -58,24 +76,38 @@
 namespace pg {
 
 namespace bf16 {
-constexpr int BM = kBf16BlockM;
 constexpr int BN = kBf16BlockN;
 constexpr int BK = kBf16BlockK;
+constexpr int kUmmaM = 128;
 constexpr int kUmmaK = 16;
-constexpr uint32_t kATileBytes = BM * BK * 2;             // 16 KiB
-constexpr uint32_t kBBoxCols = 64;                         // n per B box (128 bytes)
-constexpr uint32_t kBBoxBytes = kBBoxCols * BK * 2;        // 8 KiB
-constexpr uint32_t kBTileBytes = BN * BK * 2;              // 32 KiB
-constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 KiB
-constexpr uint32_t kTmemCols = 2 * BN;                     // two accumulators
-constexpr int kGroupM = 16;
-constexpr int kStageChunks = kStageBytes / 16;           // 3072 16-byte chunks per stage
+constexpr uint32_t kAHalfBytes = kUmmaM * BK * 2;          // 16 KiB: one 128-row half of A
+constexpr uint32_t kBBoxCols = 64;                          // n per B box (128 bytes)
+constexpr uint32_t kBBoxBytes = kBBoxCols * BK * 2;         // 8 KiB
+constexpr uint32_t kBTileBytes = BN * BK * 2;               // 32 KiB
+constexpr uint32_t kTmemCols = 512;                         // two 128 x 256 FP32 accumulators
+constexpr int kGroupRows = 2048;                            // rows of tiles per raster group
+constexpr int kEpiBoxCols = 32;                             // FP32 columns per staged store
+constexpr uint32_t kStagingBytes = 32 * kEpiBoxCols * 4;    // 4 KiB per epilogue warp
+
+// Tile of MH 128-row halves.
+template <int MH>
+struct Tile {
+    static_assert(MH == 1 || MH == 2, "one or two 128-row halves");
+    static constexpr int BM = kUmmaM * MH;
+    static constexpr uint32_t kATileBytes = kAHalfBytes * MH;
+    static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes; // 48 or 64 KiB
+    static constexpr int kStageChunks = kStageBytes / 16;
+    static constexpr int kAccBufs = 2 / MH;   // accumulators in flight
+    static constexpr int kEpiWarps = 4 * MH;  // one per 32-lane quarter and half
+    static constexpr int kGroupTiles = kGroupRows / BM;
+};
+
 // Producer warps per fill: the TMA fill needs one elected thread; the
-// thread-issued fills spread a stage's 3072 chunks over many threads (GB300,
-// 8192^3, four stages: cp.async 833 TFLOP/s with sixteen warps recomputing
-// every address, 1390 with sixteen and 1420 with eight precomputing them;
-// the register path 236 with sixteen warps in batches of two loads, 438
-// with all six of a thread's loads in flight at once).
+// thread-issued fills spread a stage's chunks over many threads (GB300,
+// 8192^3, 128-row tile, four stages: cp.async 833 TFLOP/s with sixteen warps
+// recomputing every address, 1390 with sixteen and 1420 with eight
+// precomputing them; the register path 236 with sixteen warps in batches of
+// two loads, 438 with all six of a thread's loads in flight at once).
 constexpr int kCpAsyncCopyWarps = 8;
 constexpr int kSyncCopyWarps = 16;
 
@@ -85,13 +117,13 @@ constexpr int copy_warps()
     return Fill == GEMM_FILL_TMA ? 1 : Fill == GEMM_FILL_CPASYNC ? kCpAsyncCopyWarps : kSyncCopyWarps;
 }
 
-template <int Fill>
+template <int Fill, int MH>
 struct Roles {
     static constexpr int kProducerWarps = copy_warps<Fill>();
     static constexpr int kCopyThreads = kProducerWarps * 32;
     static constexpr int kMmaWarp = kProducerWarps;
-    static constexpr int kEpiWarp0 = kMmaWarp + 1;        // four epilogue warps
-    static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+    static constexpr int kEpiWarp0 = kMmaWarp + 1;
+    static constexpr int kThreads = (kEpiWarp0 + Tile<MH>::kEpiWarps) * 32;
     static constexpr uint32_t kFullArrivals = Fill == GEMM_FILL_TMA ? 1u : static_cast<uint32_t>(kCopyThreads);
 };
 
@@ -99,7 +131,7 @@ struct Roles {
 // (bits 7-9 = 1), B = BF16 (bits 10-12 = 1), A K-major (bit 15 = 0), B
 // MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+                            (static_cast<uint32_t>(kUmmaM >> 4) << 24);
 
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
 // byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), descriptor
@@ -115,28 +147,30 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     return d;
 }
 
+template <int MH>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb)
 {
-    const int per_group = kGroupM * tiles_n;
+    constexpr int kGroup = Tile<MH>::kGroupTiles;
+    const int per_group = kGroup * tiles_n;
     const int group = t / per_group;
-    const int first_m = group * kGroupM;
-    const int gm = min(kGroupM, tiles_m - first_m);
+    const int first_m = group * kGroup;
+    const int gm = min(kGroup, tiles_m - first_m);
     const int r = t - group * per_group;
     mb = first_m + r % gm;
     nb = r / gm;
 }
-} // namespace bf16
 
-namespace bf16 {
-// 16-byte chunk q (0 .. 3071) of the stage for tile (mb, nb), K block kb:
-// chunks 0..1023 are the A box (row r = q/8 of 128, chunk c = q%8 of the
+// 16-byte chunk q of the stage for tile (mb, nb), K block kb: chunks
+// 0 .. 8 BM - 1 are the A box (row r = q/8 of BM, chunk c = q%8 of the
 // 128-byte K row), the rest the four B boxes (box j, K row r of 64, chunk c
 // of the 128-byte N row).  Gives the global element (row, col) of the
 // chunk's first value, whether it is an A chunk, and its byte offset in the
 // 128-byte-swizzled stage.
+template <int MH>
 __device__ __forceinline__ void stage_chunk(int q, int mb, int nb, int kb, int &grow, int &gcol, bool &is_a,
                                             uint32_t &dst)
 {
+    constexpr int BM = Tile<MH>::BM;
     if (q < BM * 8) {
         const int r = q >> 3, c = q & 7;
         is_a = true;
@@ -149,7 +183,7 @@ __device__ __forceinline__ void stage_chunk(int q, int mb, int nb, int kb, int &
         is_a = false;
         grow = kb * BK + r;
         gcol = nb * BN + j * static_cast<int>(kBBoxCols) + c * 8;
-        dst = kATileBytes + static_cast<uint32_t>(j) * kBBoxBytes +
+        dst = Tile<MH>::kATileBytes + static_cast<uint32_t>(j) * kBBoxBytes +
               static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
     }
 }
@@ -175,20 +209,23 @@ __device__ __forceinline__ uint4 load_chunk_bf16(const uint16_t *__restrict__ ba
 }
 } // namespace bf16
 
-template <int Fill, int S>
-__global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
+template <int Fill, int S, int MH>
+__global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        const Bf16Args p)
+                        const __grid_constant__ CUtensorMap map_c, const Bf16Args p)
 {
     using namespace bf16;
-    using R = Roles<Fill>;
+    using R = Roles<Fill, MH>;
+    using T = Tile<MH>;
+    constexpr int BM = T::BM;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align_smem(raw, 1024);
-    const uint32_t bars = base + S * kStageBytes;
+    const uint32_t staging0 = base + S * T::kStageBytes; // kEpiWarps x 4 KiB, 1024-byte aligned
+    const uint32_t bars = staging0 + T::kEpiWarps * kStagingBytes;
     const TmaRing<S> ring{bars, bars + 8u * S};
-    const uint32_t tmem_full0 = bars + 16u * S; // [2]
-    const uint32_t tmem_empty0 = tmem_full0 + 16u; // [2]
+    const uint32_t tmem_full0 = bars + 16u * S;    // [kAccBufs]
+    const uint32_t tmem_empty0 = tmem_full0 + 16u; // [kAccBufs]
     const uint32_t epi_done = tmem_empty0 + 16u;
     const uint32_t mma_done = epi_done + 8u;
     const uint32_t tmem_slot = mma_done + 8u;
@@ -203,11 +240,11 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         ring.init(1, R::kFullArrivals);
-        mbar_init(tmem_full0, 1);
-        mbar_init(tmem_full0 + 8u, 1);
-        mbar_init(tmem_empty0, 4);
-        mbar_init(tmem_empty0 + 8u, 4);
-        mbar_init(epi_done, 4);
+        for (int b = 0; b < T::kAccBufs; ++b) {
+            mbar_init(tmem_full0 + 8u * b, 1);
+            mbar_init(tmem_empty0 + 8u * b, T::kEpiWarps);
+        }
+        mbar_init(epi_done, T::kEpiWarps);
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
@@ -229,20 +266,20 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int mb, nb;
-                tile_coords(t, tiles_m, tiles_n, mb, nb);
+                tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
                 for (int kb = 0; kb < k_blocks; ++kb, ++f) {
                     if (!ring.producer_acquire(f, p.wait_limit_ns)) {
                         record_error(p.status, kErrFamilyBf16 | kErrRoleProducer);
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
+                    const uint32_t dst = base + static_cast<uint32_t>(f % S) * T::kStageBytes;
                     const uint32_t full = ring.full_bar(f);
-                    ring.producer_commit(f, kStageBytes);
+                    ring.producer_commit(f, T::kStageBytes);
                     tma_load_2d(dst, &map_a, full, kb * BK, mb * BM);
 #pragma unroll
                     for (int j = 0; j < BN / static_cast<int>(kBBoxCols); ++j)
-                        tma_load_2d(dst + kATileBytes + j * kBBoxBytes, &map_b, full,
+                        tma_load_2d(dst + T::kATileBytes + j * kBBoxBytes, &map_b, full,
                                     nb * BN + j * static_cast<int>(kBBoxCols), kb * BK);
                 }
             }
@@ -265,11 +302,12 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
         int f = 0;
         bool ok = true;
         constexpr int kCopyThreads = R::kCopyThreads;
+        constexpr int kStageChunks = T::kStageChunks;
         constexpr int kChunksPerThread = kStageChunks / kCopyThreads;
         static_assert(kStageChunks % kCopyThreads == 0, "whole chunks per thread");
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int mb, nb;
-            tile_coords(t, tiles_m, tiles_n, mb, nb);
+            tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
             // An interior tile's chunks: the same shared-memory offsets in
             // every stage, sources that advance by a fixed step per K block.
             const bool tile_interior = (mb + 1) * BM <= p.M && (nb + 1) * BN <= p.N;
@@ -281,7 +319,7 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                 for (int i = 0; i < kChunksPerThread; ++i) {
                     int grow, gcol;
                     bool is_a;
-                    stage_chunk(ptid + i * kCopyThreads, mb, nb, 0, grow, gcol, is_a, c_off[i]);
+                    stage_chunk<MH>(ptid + i * kCopyThreads, mb, nb, 0, grow, gcol, is_a, c_off[i]);
                     c_src[i] = is_a ? p.A + static_cast<long long>(grow) * p.lda + gcol
                                     : p.B + static_cast<long long>(grow) * p.ldb + gcol;
                     c_step[i] = is_a ? static_cast<long long>(BK) : static_cast<long long>(BK) * p.ldb;
@@ -295,7 +333,7 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t dst = base + static_cast<uint32_t>(f % S) * kStageBytes;
+                const uint32_t dst = base + static_cast<uint32_t>(f % S) * T::kStageBytes;
                 if constexpr (Fill == GEMM_FILL_CPASYNC) {
                     if (tile_interior && (kb + 1) * BK <= p.K) {
                         // Every chunk is a whole in-range 16-byte copy (the
@@ -310,7 +348,7 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                             int grow, gcol;
                             bool is_a;
                             uint32_t off;
-                            stage_chunk(q, mb, nb, kb, grow, gcol, is_a, off);
+                            stage_chunk<MH>(q, mb, nb, kb, grow, gcol, is_a, off);
                             const uint16_t *gbase = is_a ? p.A : p.B;
                             const long long ld = is_a ? p.lda : p.ldb;
                             const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
@@ -357,7 +395,7 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                         for (int b = 0; b < kBatch; ++b) {
                             int grow, gcol;
                             bool is_a;
-                            stage_chunk(q0 + b * kCopyThreads, mb, nb, kb, grow, gcol, is_a, off[b]);
+                            stage_chunk<MH>(q0 + b * kCopyThreads, mb, nb, kb, grow, gcol, is_a, off[b]);
                             v[b] = is_a ? load_chunk_bf16(p.A, p.lda, grow, gcol, p.M, p.K)
                                         : load_chunk_bf16(p.B, p.ldb, grow, gcol, p.K, p.N);
                         }
@@ -387,14 +425,14 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
             int local = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-                const int slot = local & 1;
-                const uint32_t use_parity = static_cast<uint32_t>((local >> 1) & 1);
+                const int slot = local % T::kAccBufs;
+                const uint32_t use_parity = static_cast<uint32_t>((local / T::kAccBufs) & 1);
                 if (!mbar_wait_bounded(tmem_empty0 + 8u * slot, use_parity ^ 1u, p.wait_limit_ns)) {
                     record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * MH * BN);
                 for (int kb = 0; kb < k_blocks; ++kb, ++f) {
                     if (!ring.consumer_wait(f, p.wait_limit_ns)) {
                         record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
@@ -402,13 +440,17 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = base + static_cast<uint32_t>(f % S) * kStageBytes;
-                    const uint32_t b_addr = a_addr + kATileBytes;
+                    const uint32_t a_addr = base + static_cast<uint32_t>(f % S) * T::kStageBytes;
+                    const uint32_t b_addr = a_addr + T::kATileBytes;
 #pragma unroll
                     for (int ks = 0; ks < BK / kUmmaK; ++ks) {
-                        const uint64_t adesc = smem_desc_sw128(a_addr + ks * kUmmaK * 2, 16, 1024);
                         const uint64_t bdesc = smem_desc_sw128(b_addr + ks * kUmmaK * 128, kBBoxBytes, 1024);
-                        mma_f16_ss(d_tmem, adesc, bdesc, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < MH; ++h) {
+                            const uint64_t adesc = smem_desc_sw128(a_addr + h * kAHalfBytes + ks * kUmmaK * 2, 16, 1024);
+                            mma_f16_ss(d_tmem + static_cast<uint32_t>(h * BN), adesc, bdesc, kIdesc,
+                                       (kb | ks) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(ring.empty_bar(f)); // stage free once these MMAs have read it
                 }
@@ -429,12 +471,16 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
         tmem_dealloc(tmem_base, kTmemCols);
     } else if (warp >= R::kEpiWarp0) {
         // ------------------------------------------------------- epilogue
-        const int quarter = warp & 3; // tensor-memory lanes 32*quarter .. +31
+        // Warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the quarter
+        // its warp index allows) of half h.
+        const int quarter = warp & 3;
+        const int half = (warp - R::kEpiWarp0) / 4;
+        const uint32_t staging = staging0 + static_cast<uint32_t>(warp - R::kEpiWarp0) * kStagingBytes;
         const bool c_vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
         int local = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-            const int slot = local & 1;
-            const uint32_t use_parity = static_cast<uint32_t>((local >> 1) & 1);
+            const int slot = local % T::kAccBufs;
+            const uint32_t use_parity = static_cast<uint32_t>((local / T::kAccBufs) & 1);
             const bool ok = mbar_wait_bounded(tmem_full0 + 8u * slot, use_parity, p.wait_limit_ns);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0)
@@ -443,20 +489,41 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
             }
             tc_fence_after_sync();
             int mb, nb;
-            tile_coords(t, tiles_m, tiles_n, mb, nb);
-            const int row = mb * BM + quarter * 32 + lane;
+            tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
+            const int row0 = mb * BM + half * kUmmaM + quarter * 32; // first row of this warp's box
+            const int row = row0 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(slot * BN);
+                                   static_cast<uint32_t>((slot * MH + half) * BN);
             float *crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = nb * BN + c * 32;
+            for (int c = 0; c < BN / kEpiBoxCols; ++c) {
+                const int col0 = nb * BN + c * kEpiBoxCols;
                 if (col0 >= p.N)
                     break; // warp-uniform
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), r);
+                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * kEpiBoxCols), r);
                 tmem_ld_wait();
-                if (row < p.M) {
+                if (row0 >= p.M)
+                    continue; // warp-uniform: the whole box lies below the matrix
+                if (p.c_tma) {
+                    // The previous box's store must have read the staging
+                    // buffer before it is overwritten.
+                    if (lane == 0)
+                        bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                                         staging + static_cast<uint32_t>(lane * 128 + ((j ^ (lane & 7)) << 4))),
+                                     "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_c, staging, col0, row0);
+                        bulk_commit_group();
+                    }
+                } else if (row < p.M) {
                     if (c_vec && col0 + 32 <= p.N) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -471,11 +538,15 @@ __global__ void __launch_bounds__(bf16::Roles<Fill>::kThreads, 1)
                     }
                 }
             }
+            // The accumulator has been read (tcgen05.wait::ld above); the
+            // stores still in flight read only the staging buffer.
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(tmem_empty0 + 8u * slot);
         }
+        if (lane == 0)
+            bulk_wait_group<0>(); // every store of this warp has written C
         __syncwarp();
         if (lane == 0)
             mbar_arrive(epi_done);
@@ -490,15 +561,17 @@ __global__ void gemm_bf16_zero_kernel(float *C, int M, int N, long long ldc)
         C[(idx / N) * ldc + idx % N] = 0.0f;
 }
 
-template <int Fill, int S>
+template <int Fill, int S, int MH>
 static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
 {
     using namespace bf16;
+    using T = Tile<MH>;
     alignas(64) CUtensorMap map_a;
     alignas(64) CUtensorMap map_b;
+    alignas(64) CUtensorMap map_c;
     if constexpr (Fill == GEMM_FILL_TMA) {
         int st = encode_tensor_map_2d(&map_a, 1, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                                      static_cast<uint64_t>(a.lda) * 2u, BK, BM, 1);
+                                      static_cast<uint64_t>(a.lda) * 2u, BK, T::BM, 1);
         if (st != GEMM_OK)
             return st;
         st = encode_tensor_map_2d(&map_b, 1, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
@@ -510,41 +583,64 @@ static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
         std::memset(&map_a, 0, sizeof map_a);
         std::memset(&map_b, 0, sizeof map_b);
     }
-    const int smem = bf16_smem_bytes(S);
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<Fill, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (a.c_tma) {
+        // C as FP32 rows, 32 x 32 boxes, 128-byte swizzle (the staging layout).
+        const int st = encode_tensor_map_2d(&map_c, 0, a.C, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+                                            static_cast<uint64_t>(a.ldc) * 4u, kEpiBoxCols, 32, 1);
+        if (st != GEMM_OK)
+            return st;
+    } else {
+        std::memset(&map_c, 0, sizeof map_c);
+    }
+    const int smem = bf16_smem_bytes(S, T::BM);
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<Fill, S, MH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return GEMM_ERR_CUDA;
-    const long long tiles = static_cast<long long>((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+    const long long tiles = static_cast<long long>((a.M + T::BM - 1) / T::BM) * ((a.N + BN - 1) / BN);
     const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);
-    gemm_bf16_tc_kernel<Fill, S><<<grid, Roles<Fill>::kThreads, smem, s>>>(map_a, map_b, a);
+    gemm_bf16_tc_kernel<Fill, S, MH><<<grid, Roles<Fill, MH>::kThreads, smem, s>>>(map_a, map_b, map_c, a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-int bf16_threads(int fill)
+int bf16_threads(int fill, int block_m)
 {
+    using namespace bf16;
+    if (block_m == 256) {
+        if (fill == GEMM_FILL_TMA)
+            return Roles<GEMM_FILL_TMA, 2>::kThreads;
+        return fill == GEMM_FILL_CPASYNC ? Roles<GEMM_FILL_CPASYNC, 2>::kThreads : Roles<GEMM_FILL_SYNC, 2>::kThreads;
+    }
     if (fill == GEMM_FILL_TMA)
-        return bf16::Roles<GEMM_FILL_TMA>::kThreads;
-    return fill == GEMM_FILL_CPASYNC ? bf16::Roles<GEMM_FILL_CPASYNC>::kThreads : bf16::Roles<GEMM_FILL_SYNC>::kThreads;
+        return Roles<GEMM_FILL_TMA, 1>::kThreads;
+    return fill == GEMM_FILL_CPASYNC ? Roles<GEMM_FILL_CPASYNC, 1>::kThreads : Roles<GEMM_FILL_SYNC, 1>::kThreads;
+}
+
+template <int Fill, int MH>
+static int launch_bf16_ring(const Bf16Args &a, cudaStream_t s)
+{
+    switch (a.stages) {
+    case 2: return launch_bf16_t<Fill, 2, MH>(a, s);
+    case 3: return launch_bf16_t<Fill, 3, MH>(a, s);
+    case 4:
+        if constexpr (MH == 1)
+            return launch_bf16_t<Fill, 4, MH>(a, s);
+        else
+            return GEMM_ERR_INVALID_ARG; // four 64 KiB stages do not fit
+    default: return GEMM_ERR_INVALID_ARG;
+    }
 }
 
 int launch_bf16(const Bf16Args &a, int fill, cudaStream_t s)
 {
-    if (fill == GEMM_FILL_SYNC)
-        return a.stages == 1 ? launch_bf16_t<GEMM_FILL_SYNC, 1>(a, s) : GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_CPASYNC) {
-        switch (a.stages) {
-        case 2: return launch_bf16_t<GEMM_FILL_CPASYNC, 2>(a, s);
-        case 3: return launch_bf16_t<GEMM_FILL_CPASYNC, 3>(a, s);
-        case 4: return launch_bf16_t<GEMM_FILL_CPASYNC, 4>(a, s);
-        default: return GEMM_ERR_INVALID_ARG;
-        }
+    const bool tall = a.block_m == 256;
+    if (fill == GEMM_FILL_SYNC) {
+        if (a.stages != 1)
+            return GEMM_ERR_INVALID_ARG;
+        return tall ? launch_bf16_t<GEMM_FILL_SYNC, 1, 2>(a, s) : launch_bf16_t<GEMM_FILL_SYNC, 1, 1>(a, s);
     }
-    switch (a.stages) {
-    case 2: return launch_bf16_t<GEMM_FILL_TMA, 2>(a, s);
-    case 3: return launch_bf16_t<GEMM_FILL_TMA, 3>(a, s);
-    case 4: return launch_bf16_t<GEMM_FILL_TMA, 4>(a, s);
-    default: return GEMM_ERR_INVALID_ARG;
-    }
+    if (fill == GEMM_FILL_CPASYNC)
+        return tall ? launch_bf16_ring<GEMM_FILL_CPASYNC, 2>(a, s) : launch_bf16_ring<GEMM_FILL_CPASYNC, 1>(a, s);
+    return tall ? launch_bf16_ring<GEMM_FILL_TMA, 2>(a, s) : launch_bf16_ring<GEMM_FILL_TMA, 1>(a, s);
 }
 
 int launch_bf16_zero(const Bf16Args &a, cudaStream_t s)

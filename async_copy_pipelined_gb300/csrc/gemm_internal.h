@@ -36,6 +36,8 @@ struct Bf16Args {
     float *C;
     long long ldc;
     int stages;
+    int block_m;  // 128 or 256 rows per CTA tile
+    int c_tma;    // 1: C is written by TMA stores (16-byte aligned C, ldc % 4 == 0)
     unsigned int *status;
     unsigned long long wait_limit_ns;
     int num_sms;
@@ -54,8 +56,8 @@ int launch_selftest_wait(unsigned int *status, unsigned long long limit_ns, cuda
 // Shared-memory bytes the FP32 kernels request for (tile, fill, stages).
 int f32_smem_bytes(int tile, int fill, int stages);
 int f32_threads(int tile, int fill);
-int bf16_smem_bytes(int stages);
-int bf16_threads(int fill);
+int bf16_smem_bytes(int stages, int block_m);
+int bf16_threads(int fill, int block_m);
 constexpr int kBf16BlockM = 128;
 constexpr int kBf16BlockN = 256;
 constexpr int kBf16BlockK = 64;

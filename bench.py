@@ -45,7 +45,10 @@ NOMINAL_BF16_DENSE_TFLOPS = 2250.0   # GB300 dense BF16, without 2:4 sparsity
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 256 << 20              # > 2x the 126 MiB L2
-DEFAULT_LEG = {"f32": dict(fill="tma", stages=4, tile=128), "bf16": dict(fill="tma", stages=4, tile=0)}
+# BF16: stages 0 and tile 0 take the library's choice for the workload (at
+# 8192^3 the 256-row tile with three stages); the plan resolves both before
+# anything is timed, so the JSON line names what ran.
+DEFAULT_LEG = {"f32": dict(fill="tma", stages=4, tile=128), "bf16": dict(fill="tma", stages=0, tile=0)}
 
 
 # --------------------------------------------------------------------- dist
@@ -308,7 +311,7 @@ def to_device(x, cols, dev):
 
 def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile):
     if name.startswith("bf16"):
-        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages)
+        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile)
     return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile)
 
 
@@ -478,6 +481,9 @@ def run_ours(args, dist: Dist):
         leg["stages"] = 1
     w, A, B = load_workload(name)
     M, N, K = w["M"], w["N"], w["K"]
+    if is_bf16:
+        plan = pg.plan_bf16(M, N, K, lda=w["lda"], fill=leg["fill"], stages=leg["stages"], block_m=leg["tile"])
+        leg["stages"], leg["tile"] = plan["stages"], plan["block_m"]
     if leg["fill"] == "tma" and not is_bf16 and w["lda"] % 4:
         # TMA cannot describe a row pitch that is not a multiple of 16 bytes;
         # the same logical matrix is repacked at the next legal pitch.
@@ -491,19 +497,21 @@ def run_ours(args, dist: Dist):
     call = gemm_call(pg, name, Ad, Bd, Cd, leg["fill"], leg["stages"], leg["tile"])
 
     # Correctness gate before any timing (the lesson program's rule): the
-    # pipelined result must be bit-identical to the register-path fill.
+    # pipelined result must be bit-identical to the register-path fill (for
+    # BF16 on the 128-row tile, so the gate also crosses tile heights).
     call()
-    gate = {"checked": False}
-    if not is_bf16:
-        Cs = torch.empty_like(Cd)
+    Cs = torch.empty_like(Cd)
+    if is_bf16:
+        pg.gemm_bf16(Ad, Bd, Cs, fill="sync", block_m=128)
+    else:
         pg.gemm_f32(Ad, Bd, Cs, fill="sync", block_tile=leg["tile"])
-        torch.cuda.synchronize()
-        gate = {"checked": True, "bit_identical_to_sync_fill": bool(torch.equal(Cd.view(torch.int32),
-                                                                                Cs.view(torch.int32)))}
-        del Cs
-        if not gate["bit_identical_to_sync_fill"]:
-            print(json.dumps({"error": "pipelined fill differs from the sync fill", "config": leg}), flush=True)
-            return 1
+    torch.cuda.synchronize()
+    gate = {"checked": True, "bit_identical_to_sync_fill": bool(torch.equal(Cd.view(torch.int32),
+                                                                            Cs.view(torch.int32)))}
+    del Cs
+    if not gate["bit_identical_to_sync_fill"]:
+        print(json.dumps({"error": "pipelined fill differs from the sync fill", "config": leg}), flush=True)
+        return 1
     st, detail = pg.device_status()
     if st != 0:
         print(json.dumps({"error": f"device status {st} ({detail:#x})"}), flush=True)
@@ -594,23 +602,28 @@ def run_ours(args, dist: Dist):
             Abd, Bbd = to_device(Ab, wb["K"], dev), to_device(Bb, wb["N"], dev)
             Cbd = torch.empty((wb["M"], wb["N"]), dtype=torch.float32, device=dev)
             fb = 2.0 * wb["M"] * wb["N"] * wb["K"]
-            cb = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", 4, 0)
+            pb = pg.plan_bf16(wb["M"], wb["N"], wb["K"], lda=wb["lda"])
+            cb = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", pb["stages"], pb["block_m"])
             mean, best, med = time_kernel(pg, cb, flush, args.sweep_launches)
             launches += args.sweep_launches
             tf = fb / (mean / 1e3) / 1e12
-            extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "ms_median": med, "stages": 4,
+            extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "ms_median": med,
+                                   "stages": pb["stages"], "block_m": pb["block_m"],
                                    "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak,
                                                 "unit": UNIT, "frac": tf / bf16_peak,
                                                 "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"},
                                    "frac_nominal_dense_2250": tf / NOMINAL_BF16_DENSE_TFLOPS}
             bfills = {}
-            for f, s in (("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 4), ("sync", 1)):
-                c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, f, s, 0)
+            for f, s, t in (("tma", 2, 128), ("tma", 3, 128), ("tma", 4, 128), ("cpasync", 2, 128),
+                            ("cpasync", 4, 128), ("sync", 1, 128), ("tma", 2, 256), ("tma", 3, 256),
+                            ("cpasync", 2, 256), ("cpasync", 3, 256), ("sync", 1, 256)):
+                c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, f, s, t)
                 m2, b2, md2 = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
-                bfills[f"{f}/S{s}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2, "ms_median": md2}
+                bfills[f"{f}/S{s}/T{t}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2,
+                                            "ms_median": md2}
             for v in bfills.values():
-                v["t_sync_over_t"] = bfills["sync/S1"]["ms"] / v["ms"]
+                v["t_sync_over_t"] = bfills["sync/S1/T128"]["ms"] / v["ms"]
             extras["bf16_8192"]["fills"] = bfills
             del Abd, Bbd, Cbd
     sampler.stop()
@@ -628,7 +641,7 @@ def run_ours(args, dist: Dist):
         Bh = Bh.pin_memory()
         Ch = torch.empty((M, N), dtype=torch.float32).pin_memory()
         if is_bf16:
-            host_call = lambda: pg.gemm_bf16(Ah, Bh, Ch, stages=leg["stages"])  # noqa: E731
+            host_call = lambda: pg.gemm_bf16(Ah, Bh, Ch, stages=leg["stages"], block_m=leg["tile"])  # noqa: E731
         else:
             host_call = lambda: pg.gemm_f32(Ah, Bh, Ch, fill=leg["fill"], stages=leg["stages"],  # noqa: E731
                                             block_tile=leg["tile"])

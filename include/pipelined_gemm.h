@@ -164,10 +164,24 @@ int gemm_f32_plan(int M, int N, int K,
  *               GEMM_FILL_SYNC (the register path: sixteen producer warps
  *               load and store, one stage, loads and MMAs alternate).
  *               GEMM_FILL_CPASYNC_MBAR returns GEMM_ERR_UNSUPPORTED.
- *   stages      TMA / cp.async: 2..4 (4 x 48 KiB fills shared memory), or
- *               0 for the default of 4.  sync: 0 or 1.
+ *   stages      TMA / cp.async: 2..4 with the 128-row tile (4 x 48 KiB
+ *               stages fill shared memory), 2..3 with the 256-row tile
+ *               (64 KiB stages), or 0 for the tile's default (4 or 3).
+ *               sync: 0 or 1.
+ *   block_m     rows per CTA tile, every tile 256 columns wide:
+ *               128 (one 128 x 256 accumulator per tile, two in tensor
+ *               memory so a tile's stores overlap the next tile's MMAs),
+ *               256 (two 128-row MMAs share each B slice: a third less
+ *               shared-memory traffic per multiply-add, one tile in tensor
+ *               memory at a time), or 0 to let the library choose: 256
+ *               when there are at least 120 tiles of 256 x 256 and stages
+ *               is not 4, else 128.  Anything else, or 256 with 4 stages,
+ *               is GEMM_ERR_INVALID_ARG.  Every fill and both tiles give
+ *               bit-identical results.
  *   Alignment   A, B 16-byte aligned; lda, ldb multiples of 8 (16-byte row
- *               pitch), else GEMM_ERR_MISALIGNED.
+ *               pitch), else GEMM_ERR_MISALIGNED.  C needs 4-byte alignment;
+ *               a 16-byte aligned C with ldc a multiple of 4 is written by
+ *               TMA stores, any other C by plain stores.
  *   Accuracy    the tensor core's internal summation order is its own, so
  *               results are not bit-identical to a sequential sum; they
  *               match the exact-product sum within float32 rounding.
@@ -177,14 +191,14 @@ int gemm_bf16(int M, int N, int K,
               const uint16_t *A, int lda,
               const uint16_t *B, int ldb,
               float *C, int ldc,
-              int fill_mode, int stages,
+              int fill_mode, int stages, int block_m,
               void *stream);
 
 int gemm_bf16_plan(int M, int N, int K,
                    const uint16_t *A, int lda,
                    const uint16_t *B, int ldb,
                    float *C, int ldc,
-                   int fill_mode, int stages,
+                   int fill_mode, int stages, int block_m,
                    gemm_plan *plan);
 
 /* Human-readable name of a status code (static storage; never NULL). */

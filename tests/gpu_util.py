@@ -44,7 +44,7 @@ def run_f32(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, fill: str, sta
 
 
 def run_bf16(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, stages: int = 0, ldc: int | None = None,
-             sentinel: float = 12345.0, fill: str = "tma"):
+             sentinel: float = 12345.0, fill: str = "tma", block_m: int = 0):
     import torch
     import async_copy_pipelined_gb300 as pg
     Ad = to_device(A, K)
@@ -52,7 +52,7 @@ def run_bf16(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, stages: int =
     ldc = N if ldc is None else ldc
     Cbuf = torch.full((M, max(ldc, 1)), sentinel, dtype=torch.float32, device="cuda")
     C = Cbuf[:, :N]
-    pg.gemm_bf16(Ad, Bd, C, fill=fill, stages=stages)
+    pg.gemm_bf16(Ad, Bd, C, fill=fill, stages=stages, block_m=block_m)
     st, detail = pg.device_status()
     assert st == 0, f"device status {st} detail {detail:#x}"
     torch.cuda.synchronize()

@@ -138,22 +138,57 @@ def test_plan_accepts_what_only_some_fills_accept(lib):
 def test_bf16_plan(lib):
     p = pg.GemmPlan()
     L = pg.lib()
-    st = L.gemm_bf16_plan(8192, 8192, 8192, 256, 8192, 256, 8192, 256, 8192, 2, 0, ctypes.byref(p))
+    st = L.gemm_bf16_plan(8192, 8192, 8192, 256, 8192, 256, 8192, 256, 8192, 2, 0, 0, ctypes.byref(p))
     assert st == 0
     d = p.as_dict()
-    assert (d["block_m"], d["block_n"], d["block_k"], d["stages"]) == (128, 256, 64, 4)
-    assert d["smem_bytes"] <= 227 * 1024 and d["k_slices"] == 128
-    assert d["threads"] == 192 and d["a_copy_bytes"] == 16384
-    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 0, ctypes.byref(p)) == 0
+    # 1024 tiles of 256 x 256: the 256-row tile, three 64 KiB stages, eight
+    # epilogue warps with a 4 KiB staging box each.
+    assert (d["block_m"], d["block_n"], d["block_k"], d["stages"]) == (256, 256, 64, 3)
+    assert d["smem_bytes"] == 3 * 65536 + 8 * 4096 + 2048 <= 227 * 1024 and d["k_slices"] == 128
+    assert d["threads"] == (1 + 1 + 8) * 32 and d["a_copy_bytes"] == 32768
+    assert (d["grid_x"], d["grid_y"]) == (1024, 1)
+    # Four stages only fit the 128-row tile: asking for them picks it.
+    st = L.gemm_bf16_plan(8192, 8192, 8192, 256, 8192, 256, 8192, 256, 8192, 2, 4, 0, ctypes.byref(p))
+    d = p.as_dict()
+    assert st == 0 and (d["block_m"], d["stages"], d["threads"]) == (128, 4, (1 + 1 + 4) * 32)
+    assert d["smem_bytes"] == 4 * 49152 + 4 * 4096 + 2048 and d["a_copy_bytes"] == 16384
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 0, 0, ctypes.byref(p)) == 0
     d = p.as_dict()
     assert d["stages"] == 1 and d["threads"] == 672 and d["a_copy_bytes"] == 16
-    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 2, ctypes.byref(p)) == 1
-    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 1, 0, ctypes.byref(p)) == 0
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 0, 2, 0, ctypes.byref(p)) == 1
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 1, 0, 0, ctypes.byref(p)) == 0
     assert p.as_dict()["stages"] == 4 and p.as_dict()["threads"] == 416
-    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 3, 0, ctypes.byref(p)) == 3
-    assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
-    assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, ctypes.byref(p)) == 2
-    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, ctypes.byref(p)) == 1
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 3, 0, 0, ctypes.byref(p)) == 3
+    assert L.gemm_bf16_plan(64, 64, 60, 256, 60, 256, 64, 256, 64, 2, 0, 0, ctypes.byref(p)) == 2
+    assert L.gemm_bf16_plan(64, 64, 64, 258, 64, 256, 64, 256, 64, 2, 0, 0, ctypes.byref(p)) == 2
+    assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, 0, ctypes.byref(p)) == 1
+
+
+@pytest.mark.parametrize("M,N,fill,stages,block_m,want", [
+    (8192, 8192, 2, 0, 0, (256, 3)),      # enough 256 x 256 tiles: the 256-row tile
+    (2816, 2816, 2, 0, 0, (256, 3)),      # 11 x 11 = 121 tiles
+    (2560, 2816, 2, 0, 0, (128, 4)),      # 10 x 11 = 110 tiles: the 128-row tile
+    (8192, 8192, 2, 2, 0, (256, 2)),
+    (8192, 8192, 2, 4, 0, (128, 4)),      # four stages: only the 128-row tile holds them
+    (8192, 8192, 1, 0, 0, (256, 3)),      # the cp.async fill follows the same rule
+    (8192, 8192, 0, 0, 0, (256, 1)),      # and the register fill, with its one stage
+    (8192, 8192, 2, 0, 128, (128, 4)),    # an explicit tile keeps its own default depth
+    (64, 64, 2, 0, 256, (256, 3)),
+    (64, 64, 0, 1, 256, (256, 1)),
+])
+def test_bf16_plan_tile_choice(lib, M, N, fill, stages, block_m, want):
+    p = pg.GemmPlan()
+    st = pg.lib().gemm_bf16_plan(M, N, 64, 256, 64, 256, N, 256, N, fill, stages, block_m, ctypes.byref(p))
+    d = p.as_dict()
+    assert st == 0 and (d["block_m"], d["stages"]) == want
+    assert d["threads"] == ({2: 1, 1: 8, 0: 16}[fill] + 1 + 4 * (want[0] // 128)) * 32
+
+
+@pytest.mark.parametrize("fill,stages,block_m", [(2, 4, 256), (1, 4, 256), (2, 0, 64), (2, 0, 192), (2, 0, 512)])
+def test_bf16_plan_tile_refusals(lib, fill, stages, block_m):
+    p = pg.GemmPlan()
+    assert pg.lib().gemm_bf16_plan(256, 256, 64, 256, 64, 256, 256, 256, 256, fill, stages, block_m,
+                                   ctypes.byref(p)) == 1
 
 
 

@@ -61,11 +61,11 @@ def test_refusals_enqueue_nothing():
     # register-path fill has exactly one stage.
     Ab = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
     lib = pg.lib()
-    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 3, 0, None)
+    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 3, 0, 0, None)
     assert st == 3
-    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 0, 2, None)
+    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 0, 2, 0, None)
     assert st == 1
-    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 2, 6, None)
+    st = lib.gemm_bf16(64, 64, 64, Ab.data_ptr(), 64, Ab.data_ptr(), 64, C.data_ptr(), 64, 2, 6, 0, None)
     assert st == 1  # stages above what fits in shared memory
     torch.cuda.synchronize()
     assert torch.all(C == 9.0), "a refused call wrote C"

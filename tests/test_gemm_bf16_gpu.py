@@ -36,19 +36,23 @@ SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 128), (130, 300, 70), (64, 512, 
           (300, 257, 1000), (1, 700, 64), (700, 1, 64)]
 
 
-BF16_FILLS = [("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 3), ("cpasync", 4), ("sync", 1)]
+# (fill, stages, rows per CTA tile): every ring depth each tile holds.
+BF16_CASES = [("tma", 2, 128), ("tma", 3, 128), ("tma", 4, 128), ("cpasync", 2, 128), ("cpasync", 3, 128),
+              ("cpasync", 4, 128), ("sync", 1, 128),
+              ("tma", 2, 256), ("tma", 3, 256), ("cpasync", 2, 256), ("cpasync", 3, 256), ("sync", 1, 256)]
 
 
-@pytest.mark.parametrize("fill,stages", BF16_FILLS)
+@pytest.mark.parametrize("fill,stages,block_m", BF16_CASES)
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_small_ragged_normal(fill, stages, M, N, K):
+def test_small_ragged_normal(fill, stages, block_m, M, N, K):
     A, B = bf16_operands("normal", M, N, K, 60 + K)
-    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
     want = oracle.gemm_bf16_f64(A, B, M, N, K)
-    _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} {M}x{N}x{K}")
-    # Every fill feeds the same MMA sequence with the same bytes: same bits.
-    if fill != "tma":
-        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma")
+    _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} T{block_m} {M}x{N}x{K}")
+    # Every fill and tile feeds the same MMA sequence per output element with
+    # the same bytes: same bits.
+    if (fill, stages, block_m) != ("tma", 4, 128):
+        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma", block_m=128)
         np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
@@ -62,30 +66,32 @@ def _walk_case(M, N, K):
     if key not in _WALK_CACHE:
         A, B = bf16_operands("normal", M, N, K, 70 + K)
         want = oracle.gemm_bf16_f64(A, B, M, N, K)
-        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma")
+        ref, _ = run_bf16(A, B, M, N, K, stages=4, fill="tma", block_m=128)
         _WALK_CACHE[key] = (A, B, want, ref, _abs_products(A, B, M, N, K))
     return _WALK_CACHE[key]
 
 
-@pytest.mark.parametrize("fill,stages", BF16_FILLS)
-@pytest.mark.parametrize("M,N,K", [(2048, 2560, 192), (2000, 2600, 200)])
-def test_persistent_walk_interior_and_edge_tiles(fill, stages, M, N, K):
-    """160 / 176 tiles on at most 152 persistent CTAs.  The first shape has
-    only interior tiles and whole K blocks (the thread-issued fills' per-tile
-    address path throughout); the second mixes interior and edge tiles and
-    ends every tile with an 8-deep K tail (guarded path for edge tiles and for
-    the last K block)."""
+@pytest.mark.parametrize("fill,stages,block_m", BF16_CASES)
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 192), (2000, 2600, 200), (4096, 2560, 192), (4000, 2600, 200)])
+def test_persistent_walk_interior_and_edge_tiles(fill, stages, block_m, M, N, K):
+    """More tiles than the 152 persistent CTAs: 160 / 176 128-row tiles for
+    the first two shapes, 160 / 176 256-row tiles for the last two.  The
+    first shape of each pair has only interior tiles and whole K blocks (the
+    thread-issued fills' per-tile address path throughout); the second mixes
+    interior and edge tiles and ends every tile with an 8-deep K tail
+    (guarded path for edge tiles and for the last K block)."""
     A, B, want, ref, absprod = _walk_case(M, N, K)
-    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
-    _check(got, want, absprod, K, f"bf16 {fill} S{stages} {M}x{N}x{K}")
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
+    _check(got, want, absprod, K, f"bf16 {fill} S{stages} T{block_m} {M}x{N}x{K}")
     np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("fill,stages", [("tma", 4), ("cpasync", 3), ("sync", 1)])
+@pytest.mark.parametrize("fill,stages,block_m", [("tma", 4, 128), ("cpasync", 3, 128), ("sync", 1, 128),
+                                                 ("tma", 3, 256), ("cpasync", 2, 256), ("sync", 1, 256)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 500), (513, 257, 1000)])
-def test_smallint_exact(fill, stages, M, N, K):
+def test_smallint_exact(fill, stages, block_m, M, N, K):
     A, B = bf16_operands("smallint", M, N, K, 8)
-    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+    got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
     Ai = inputs.bf16_bits_to_f32(A[:, :K]).astype(np.int64)
     Bi = inputs.bf16_bits_to_f32(B[:, :N]).astype(np.int64)
     np.testing.assert_array_equal(got, (Ai @ Bi).astype(np.float32))
@@ -106,12 +112,18 @@ def test_closed_forms():
     assert np.all(got == np.float32(K))
 
 
-def test_padded_and_ldc_canary():
-    M, N, K = 200, 300, 96
+@pytest.mark.parametrize("block_m", [128, 256])
+@pytest.mark.parametrize("ldc_pad", [3, 4, 36])
+def test_padded_and_ldc_canary(block_m, ldc_pad):
+    """Padded operands, and C rows longer than N: with ldc = N + 3 rows are
+    not 16-byte aligned and the epilogue stores element by element; with
+    N + 4 and N + 36 the TMA stores must clip at column N.  The padding
+    columns must keep their sentinel."""
+    M, N, K = 300, 300, 96
     A, B = bf16_operands("normal", M, N, K, 5, lda=K + 8, ldb=N + 16)
-    got, full = run_bf16(A, B, M, N, K, ldc=N + 3, sentinel=-5.0)
+    got, full = run_bf16(A, B, M, N, K, ldc=N + ldc_pad, sentinel=-5.0, block_m=block_m)
     want = oracle.gemm_bf16_f64(A, B, M, N, K)
-    _check(got, want, _abs_products(A, B, M, N, K), K, "padded")
+    _check(got, want, _abs_products(A, B, M, N, K), K, f"padded T{block_m} ldc N+{ldc_pad}")
     assert np.all(full[:, N:] == -5.0)
 
 
@@ -148,9 +160,10 @@ def test_workload_8192_sampled():
     # the cp.async and register-path fills the same bits as the TMA fill.
     C2 = pg.gemm_bf16(Ad, Bd)
     assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
-    for fill, stages in (("cpasync", 4), ("cpasync", 2), ("sync", 1)):
-        C3 = pg.gemm_bf16(Ad, Bd, fill=fill, stages=stages)
-        assert torch.equal(C.view(torch.int32), C3.view(torch.int32)), fill
+    for fill, stages, block_m in (("tma", 4, 128), ("tma", 2, 256), ("cpasync", 4, 128), ("cpasync", 3, 256),
+                                  ("cpasync", 2, 128), ("sync", 1, 128), ("sync", 1, 256)):
+        C3 = pg.gemm_bf16(Ad, Bd, fill=fill, stages=stages, block_m=block_m)
+        assert torch.equal(C.view(torch.int32), C3.view(torch.int32)), (fill, stages, block_m)
     assert pg.device_status()[0] == 0
 
 
@@ -163,19 +176,23 @@ def test_workload_8192_smallint_exact_sampled():
     A, B = bf16_operands("smallint", M, N, K, 104)
     rows = sample_rows(M, 24, seed=104, tiles=(128,))
     want = oracle_bf16_rows(A, B, rows, N, K).astype(np.float32)
-    for fill, stages in (("tma", 4), ("cpasync", 4), ("sync", 1)):
-        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
-        np.testing.assert_array_equal(got[rows], want, err_msg=f"8192^3 small-int {fill}/S{stages}")
+    for fill, stages, block_m in (("tma", 0, 0), ("tma", 4, 128), ("cpasync", 4, 128), ("cpasync", 3, 256),
+                                  ("sync", 1, 256)):
+        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
+        np.testing.assert_array_equal(got[rows], want, err_msg=f"8192^3 small-int {fill}/S{stages}/T{block_m}")
 
 
-@pytest.mark.parametrize("fill,stages", [("tma", 4), ("tma", 2), ("cpasync", 3), ("sync", 1)])
-def test_randomized_shapes(fill, stages):
-    """Random ragged sizes and padded leading dimensions (seeded)."""
+@pytest.mark.parametrize("fill,stages,block_m", [("tma", 4, 128), ("tma", 2, 128), ("cpasync", 3, 128),
+                                                 ("sync", 1, 128), ("tma", 3, 256), ("cpasync", 2, 256),
+                                                 ("sync", 1, 256)])
+def test_randomized_shapes(fill, stages, block_m):
+    """Random ragged sizes and padded leading dimensions (seeded); N mod 4
+    decides whether C is written by TMA stores or by plain stores."""
     rng = np.random.default_rng(1234 + stages)
     for _ in range(8):
         M, N, K = (int(rng.integers(1, 400)), int(rng.integers(1, 600)), int(rng.integers(1, 300)))
         A, B = bf16_operands("normal", M, N, K, M + N + K, lda=K + int(rng.integers(0, 17)),
                              ldb=N + int(rng.integers(0, 17)))
-        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill)
+        got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
         want = oracle.gemm_bf16_f64(A, B, M, N, K)
-        _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} {M}x{N}x{K}")
+        _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} T{block_m} {M}x{N}x{K}")

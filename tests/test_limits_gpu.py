@@ -61,8 +61,9 @@ def test_f32_rows_at_the_grid_limit_with_64bit_offsets(fill, stages):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("fill,stages", [("tma", 4), ("cpasync", 4), ("sync", 1)])
-def test_bf16_rows_beyond_4gb_offsets(fill, stages):
+@pytest.mark.parametrize("fill,stages,block_m", [("tma", 4, 128), ("cpasync", 4, 128), ("sync", 1, 128),
+                                                 ("tma", 3, 256)])
+def test_bf16_rows_beyond_4gb_offsets(fill, stages, block_m):
     """M = 2^23 + 72 ragged rows, K = 256: A holds 4.3 GB of bfloat16 and C
     8.6 GB, so both the operand and the output offsets pass 2^32 bytes."""
     import torch
@@ -70,7 +71,7 @@ def test_bf16_rows_beyond_4gb_offsets(fill, stages):
     M, N, K = (1 << 23) + 72, 256, 256
     A = _smallint((M, K), 21, torch.bfloat16)
     B = _smallint((K, N), 22, torch.bfloat16)
-    C = pg.gemm_bf16(A, B, fill=fill, stages=stages)
+    C = pg.gemm_bf16(A, B, fill=fill, stages=stages, block_m=block_m)
     assert pg.device_status()[0] == 0
     rows = np.unique(np.concatenate([sample_rows(M, 16, seed=23, tiles=(128,)), np.arange(M - 140, M),
                                      [M // 2]]))
@@ -80,17 +81,19 @@ def test_bf16_rows_beyond_4gb_offsets(fill, stages):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("fill,stages", [("tma", 2), ("tma", 3), ("tma", 4), ("cpasync", 2), ("cpasync", 4),
-                                         ("sync", 1)])
-def test_bf16_long_k_wraps_the_ring(fill, stages):
+@pytest.mark.parametrize("fill,stages,block_m", [("tma", 2, 128), ("tma", 3, 128), ("tma", 4, 128),
+                                                 ("cpasync", 2, 128), ("cpasync", 4, 128), ("sync", 1, 128),
+                                                 ("tma", 2, 256), ("tma", 3, 256), ("cpasync", 3, 256)])
+def test_bf16_long_k_wraps_the_ring(fill, stages, block_m):
     """K = 65536: 1024 K blocks per tile through a ring of 1 to 4 stages,
-    i.e. hundreds of phase flips of every barrier; two tile rows and three
-    tile columns (one ragged) on persistent CTAs."""
+    i.e. hundreds of phase flips of every barrier; two 128-row tile rows (or
+    one 256-row tile row) and three tile columns (one ragged) on persistent
+    CTAs."""
     import torch
     import async_copy_pipelined_gb300 as pg
     M, N, K = 256, 600, 65536
     A = _smallint((M, K), 31, torch.bfloat16)
     B = _smallint((K, N), 32, torch.bfloat16)
-    C = pg.gemm_bf16(A, B, fill=fill, stages=stages)
+    C = pg.gemm_bf16(A, B, fill=fill, stages=stages, block_m=block_m)
     assert pg.device_status()[0] == 0
     np.testing.assert_array_equal(C.cpu().numpy(), _oracle_rows(A, B, np.arange(M)))
