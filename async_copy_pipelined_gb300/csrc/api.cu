@@ -31,8 +31,17 @@ constexpr int kDefaultStagesF32 = 4;
 // stages for the 256-row tile (four of those do not fit in 227 KiB).
 constexpr int kDefaultStagesBf16Tile128 = 4;
 constexpr int kDefaultStagesBf16Tile256 = 3;
-// block_m = 0 picks the 256-row BF16 tile from this many 256 x 256 tiles on.
-constexpr long long kBf16TallTileMinTiles = 120;
+// block_m = 0 weighs the two BF16 tiles by waves of persistent CTAs: a
+// 256-row tile does twice the work of a 128-row one at this much higher
+// throughput (per cent; GB300, 8192^3: 1881 against 1738 TFLOP/s).  The
+// model picks the faster tile on every shape measured (1536^2 .. 8192^2,
+// 512 x 16384, 1024 x 8192, 8192 x 1024); e.g. 3584^2 x 4096 keeps the
+// 128-row tile (392 tiles in 3 waves against 196 in 2 double waves:
+// measured 1341 against 1172 TFLOP/s) and 2304^2 x 4096 takes the 256-row
+// tile (910 against 822).
+constexpr long long kBf16TallTileSpeedPct = 108;
+// SM count assumed when no device can be asked (a GB300 has 152).
+constexpr int kPlanningSms = 152;
 // block_tile = 0 picks the 128x128 tile from this many 128x128 tiles on (a
 // little under one wave at one CTA per SM on a 152-SM GB300); below it the
 // 64x64 tile, three CTAs per SM, fills the GPU better.  Measured on GB300
@@ -164,6 +173,23 @@ int bf16_smem_bytes(int stages, int block_m)
 }
 
 // ------------------------------------------------------------ planning
+// SMs of the current device for choosing a tile (cached once the device has
+// been checked), or kPlanningSms where there is no device to ask.
+static int planning_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_num_sms[dev].load();
+        if (cached > 0)
+            return cached;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+            return sms;
+    }
+    (void)cudaGetLastError();
+    return kPlanningSms;
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -272,11 +298,13 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
     if (fill != GEMM_FILL_SYNC && stages != 0 && (stages < 2 || stages > kDefaultStagesBf16Tile128))
         return GEMM_ERR_INVALID_ARG;
     if (block_m == 0) {
-        // Four stages only fit the 128-row tile; otherwise the 256-row tile
-        // once there are enough of them to fill the GPU.
-        const long long tall_tiles =
-            static_cast<long long>((M + 255) / 256) * ((N + kBf16BlockN - 1) / kBf16BlockN);
-        block_m = (stages == 4 || tall_tiles < kBf16TallTileMinTiles) ? 128 : 256;
+        // Four stages only fit the 128-row tile.  Otherwise compare the time
+        // of ceil(tiles / SMs) waves of each tile.
+        const long long sms = planning_sms();
+        const long long tiles_n_ = (N + kBf16BlockN - 1) / kBf16BlockN;
+        const long long waves128 = ((static_cast<long long>(M) + 127) / 128 * tiles_n_ + sms - 1) / sms;
+        const long long waves256 = ((static_cast<long long>(M) + 255) / 256 * tiles_n_ + sms - 1) / sms;
+        block_m = (stages != 4 && 2 * waves256 * 100 < waves128 * kBf16TallTileSpeedPct) ? 256 : 128;
     }
     if (fill == GEMM_FILL_SYNC)
         stages = 1;

@@ -23,9 +23,10 @@
 // Tensor memory holds two 128 x 256 FP32 accumulators.  The 128-row tile uses
 // them as a double buffer, so the epilogue of tile i overlaps the MMAs of
 // tile i+1.  The 256-row tile uses both for one tile: each B slice then feeds
-// two MMAs, so the shared-memory bytes written by the fill and read by the
-// tensor core per multiply-add drop by a third.  Shared-memory bandwidth,
-// which those writes and reads share, is what bounds the 128-row tile
+// two MMAs, so the fill writes a third fewer shared-memory bytes per
+// multiply-add (the tensor core still reads B once per MMA, so its reads per
+// multiply-add stay the same).  Shared-memory bandwidth, which the fill's
+// writes and the tensor core's reads share, is what bounds the 128-row tile
 // (measured on GB300 at 8192^3: the MMAs alone, with no loads after the
 // first ring, run at 2140 TFLOP/s, the full kernel at 1667); the price is an
 // epilogue that no longer overlaps the next tile's MMAs.

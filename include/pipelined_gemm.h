@@ -114,8 +114,8 @@ typedef struct gemm_plan {
  *               left untouched.
  *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA or
  *               GEMM_FILL_CPASYNC_MBAR.
- *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default
- *               (see gemm_f32_plan).  Each stage is one more slice in flight
+ *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default of 4.
+ *               Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
  *               "Exercise").
  *   block_tile  64 (64x64 tile, 4x4 micro-tile per thread, 256 threads: the
@@ -171,13 +171,16 @@ int gemm_f32_plan(int M, int N, int K,
  *   block_m     rows per CTA tile, every tile 256 columns wide:
  *               128 (one 128 x 256 accumulator per tile, two in tensor
  *               memory so a tile's stores overlap the next tile's MMAs),
- *               256 (two 128-row MMAs share each B slice: a third less
- *               shared-memory traffic per multiply-add, one tile in tensor
- *               memory at a time), or 0 to let the library choose: 256
- *               when there are at least 120 tiles of 256 x 256 and stages
- *               is not 4, else 128.  Anything else, or 256 with 4 stages,
- *               is GEMM_ERR_INVALID_ARG.  Every fill and both tiles give
- *               bit-identical results.
+ *               256 (two 128-row MMAs share each B slice: the fill writes
+ *               a third fewer shared-memory bytes per multiply-add; one
+ *               tile in tensor memory at a time), or 0 to let the library
+ *               choose: 128
+ *               when stages is 4, else whichever tile needs less time for
+ *               its waves of persistent CTAs over the current device's SMs
+ *               (152 when no device can be asked), a 256-row tile counting
+ *               as 2 / 1.08 waves of the 128-row tile.  Anything else, or
+ *               256 with 4 stages, is GEMM_ERR_INVALID_ARG.  Every fill and
+ *               both tiles give bit-identical results.
  *   Alignment   A, B 16-byte aligned; lda, ldb multiples of 8 (16-byte row
  *               pitch), else GEMM_ERR_MISALIGNED.  C needs 4-byte alignment;
  *               a 16-byte aligned C with ldc a multiple of 4 is written by
@@ -194,6 +197,10 @@ int gemm_bf16(int M, int N, int K,
               int fill_mode, int stages, int block_m,
               void *stream);
 
+/* gemm_bf16_plan: validate exactly as gemm_bf16 does and describe the launch
+ * it would make.  With block_m = 0 it asks the current device for its SM
+ * count (152 if there is none); it launches nothing.  `plan` is a host
+ * pointer. */
 int gemm_bf16_plan(int M, int N, int K,
                    const uint16_t *A, int lda,
                    const uint16_t *B, int ldb,

@@ -164,10 +164,14 @@ def test_bf16_plan(lib):
     assert L.gemm_bf16_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2, 5, 0, ctypes.byref(p)) == 1
 
 
+# Without a device the planner assumes 152 SMs.  Waves of 128-row tiles w1
+# against waves of 256-row tiles w2: the 256-row tile when 2 w2 < 1.08 w1.
 @pytest.mark.parametrize("M,N,fill,stages,block_m,want", [
-    (8192, 8192, 2, 0, 0, (256, 3)),      # enough 256 x 256 tiles: the 256-row tile
-    (2816, 2816, 2, 0, 0, (256, 3)),      # 11 x 11 = 121 tiles
-    (2560, 2816, 2, 0, 0, (128, 4)),      # 10 x 11 = 110 tiles: the 128-row tile
+    (8192, 8192, 2, 0, 0, (256, 3)),      # w1 = 14, w2 = 7
+    (2304, 2304, 2, 0, 0, (256, 3)),      # 162 tiles in 2 waves against 81 in 1
+    (2048, 2048, 2, 0, 0, (128, 4)),      # 128 tiles in 1 wave against 64 in 1
+    (3584, 3584, 2, 0, 0, (128, 4)),      # 392 tiles in 3 waves against 196 in 2
+    (1024, 8192, 2, 0, 0, (256, 3)),      # 256 tiles in 2 waves against 128 in 1
     (8192, 8192, 2, 2, 0, (256, 2)),
     (8192, 8192, 2, 4, 0, (128, 4)),      # four stages: only the 128-row tile holds them
     (8192, 8192, 1, 0, 0, (256, 3)),      # the cp.async fill follows the same rule
