@@ -46,6 +46,15 @@ struct F32Tile {
     static constexpr int kThreadCols = BN / TN;
     static constexpr int kThreadRows = BM / TM;
     static constexpr int kThreads = kThreadCols * kThreadRows;
+    // How many k ahead of its use the cp.async fills load a B fragment.  A
+    // one-warp CTA has no other warp to cover a shared load's latency, its
+    // warp also issues the copies, and the 8x4 tile's 16 paired FMAs per k
+    // are too few to hide it: there B is loaded two k ahead (measured on
+    // GB300, 32x32x65536, four stages: cp.async 1926 -> 1819 us, cp.async +
+    // mbarrier 2477 -> 2420 us).  The TMA and register-path fills gain
+    // nothing from it (TMA S2 / S4 unchanged, six stages slower), and a third
+    // k ahead costs more registers than it hides.
+    static constexpr int kBDistCpAsync = kThreads == 32 ? 2 : 1;
     static constexpr int kColGroups = TN / 4;
     static constexpr int kColGroupStride = BN / kColGroups;
     static constexpr int kAFloats = BM * BK;
@@ -156,10 +165,11 @@ __device__ __forceinline__ void load_b_frag(const float *__restrict__ sB, int tc
 // ascending k, whichever fill staged the slice, so every fill gives the same
 // bits.
 //
-// The fragment registers are double buffered: the B fragment of k+1 and the
-// A fragment of the next four k are loaded while the FMAs of k run, so
-// shared-memory latency hides behind 32 paired FMAs per k.  They also live
-// across slices: prime() loads k = 0 of the first slice, and run() computes
+// The fragment registers are double buffered: the B fragment of k+BDist
+// (BDist + 1 buffers) and the A fragment of the next four k are loaded
+// while the FMAs of k run, so shared-memory latency hides behind the paired
+// FMAs of k.  They also live
+// across slices: prime() loads the first k of a slice, and run() computes
 // one slice.  At the start of its last k every shared-memory read of the
 // slice has been issued, so run() calls `release` (the stage may be refilled)
 // and then asks `next` for the following slice's stage (nullptr if there is
@@ -167,15 +177,19 @@ __device__ __forceinline__ void load_b_frag(const float *__restrict__ sB, int tc
 // into the buffers k = 16 would use.  A consumer that waits for the next slice
 // inside `next` thus overlaps the wait and the first shared loads of slice
 // kt+1 with the FMAs of slice kt, without holding slice kt's stage.
-template <class T>
+template <class T, int BDist = 1>
 struct FragPipe {
+    static constexpr int kBBufs = BDist + 1;
+    static_assert(!T::kChainSlices || BDist == 1, "a chained slice loads B one k ahead");
     float4 a[2][T::TM];
-    unsigned long long b[2][T::TN / 2];
+    unsigned long long b[kBBufs][T::TN / 2];
 
     __device__ __forceinline__ void prime(const float *__restrict__ sA, const float *__restrict__ sB, int tr, int tc)
     {
         load_a_frag<T>(sA, tr, 0, a[0]);
-        load_b_frag<T>(sB, tc, 0, b[0]);
+#pragma unroll
+        for (int d = 0; d < BDist; ++d)
+            load_b_frag<T>(sB, tc, d, b[d]);
     }
 
     template <class Release, class Next>
@@ -196,19 +210,19 @@ struct FragPipe {
 #pragma unroll
         for (int k = 0; k < T::BK; ++k) {
             const int ab = (k / 4) & 1;
-            const int bb = k & 1;
+            const int bb = k % kBBufs;
             if (k == T::BK / 2)
                 mid();
             if ((k & 3) == 0 && k + 4 < T::BK)
                 load_a_frag<T>(sA, tr, k / 4 + 1, a[ab ^ 1]);
-            if (k + 1 < T::BK)
-                load_b_frag<T>(sB, tc, k + 1, b[bb ^ 1]);
+            if (k + BDist < T::BK)
+                load_b_frag<T>(sB, tc, k + BDist, b[(k + BDist) % kBBufs]);
             if (k + 1 == T::BK) {
                 release();
                 nA = next();
                 if (nA) {
                     load_a_frag<T>(nA, tr, 0, a[ab ^ 1]);
-                    load_b_frag<T>(nA + T::kAFloats, tc, 0, b[bb ^ 1]);
+                    load_b_frag<T>(nA + T::kAFloats, tc, 0, b[(k + 1) % kBBufs]);
                 }
             }
 #pragma unroll

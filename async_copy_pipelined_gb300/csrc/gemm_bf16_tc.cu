@@ -477,7 +477,6 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
         const int quarter = warp & 3;
         const int half = (warp - R::kEpiWarp0) / 4;
         const uint32_t staging = staging0 + static_cast<uint32_t>(warp - R::kEpiWarp0) * kStagingBytes;
-        const bool c_vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
         int local = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
             const int slot = local % T::kAccBufs;
@@ -525,18 +524,12 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                         bulk_commit_group();
                     }
                 } else if (row < p.M) {
-                    if (c_vec && col0 + 32 <= p.N) {
+                    // C is not 16-byte aligned or ldc not a multiple of 4
+                    // (otherwise TMA stores write it): one guarded float each.
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<float4 *>(crow + col0 + 4 * j) =
-                                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N)
-                                crow[col0 + j] = __uint_as_float(r[j]);
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < p.N)
+                            crow[col0 + j] = __uint_as_float(r[j]);
                 }
             }
             // The accumulator has been read (tcgen05.wait::ld above); the

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
         __syncthreads();        // ... and everyone's; slice kt-1 fully consumed
         const int fetch = kt + S - 1;
         const float *sA = smem + (kt % S) * T::kStageFloats;
-        FragPipe<T> frag;
+        FragPipe<T, T::kBDistCpAsync> frag;
         frag.prime(sA, sA + T::kAFloats, tr, tc);
         // The refill of the stage slice kt-1 used is issued halfway through
         // slice kt's FMAs, where it takes otherwise idle issue slots, rather

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
             record_error(p.status, kErrFamilyF32CpAsyncMbar | kErrRoleConsumer);
         return false;
     };
-    FragPipe<T> frag;
+    FragPipe<T, T::kBDistCpAsync> frag;
     auto refill = [&](int fetch) {
         if (fetch >= k_slices)
             return true;
