@@ -607,11 +607,15 @@ def run_ours(args, dist: Dist):
             mean, best, med = time_kernel(pg, cb, flush, args.sweep_launches)
             launches += args.sweep_launches
             tf = fb / (mean / 1e3) / 1e12
+            roof_b = {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": UNIT, "frac": tf / bf16_peak,
+                      "traffic": profiled_traffic(f"bf16_8192:tma/S{pb['stages']}/T{pb['block_m']}"),
+                      "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"}
+            if roof_b["traffic"]:
+                hbm_b = float(peaks.get("hbm_gbs") or 0.0)
+                roof_b["dram_gbs"] = roof_b["traffic"] / (mean / 1e3) / 1e9
+                roof_b["dram_frac_of_hbm"] = roof_b["dram_gbs"] / hbm_b if hbm_b else None
             extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "ms_median": med,
-                                   "stages": pb["stages"], "block_m": pb["block_m"],
-                                   "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak,
-                                                "unit": UNIT, "frac": tf / bf16_peak,
-                                                "peak_source": f"{peaks['_source']} cuBLAS bf16 burst"},
+                                   "stages": pb["stages"], "block_m": pb["block_m"], "roofline": roof_b,
                                    "frac_nominal_dense_2250": tf / NOMINAL_BF16_DENSE_TFLOPS}
             bfills = {}
             for f, s, t in (("tma", 2, 128), ("tma", 3, 128), ("tma", 4, 128), ("cpasync", 2, 128),
