@@ -21,7 +21,7 @@ import threading
 
 __all__ = [
     "FILL", "GemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "plan_f32", "plan_bf16",
-    "device_status", "selftest_bounded_wait", "status_string", "build",
+    "device_status", "selftest_bounded_wait", "testing_set_hooks", "status_string", "build",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +79,8 @@ def _bind(l):
     l.gemm_selftest_bounded_wait.restype = I
     l.gemm_version.argtypes = []
     l.gemm_version.restype = I
+    l.gemm_testing_set_hooks.argtypes = [ctypes.c_ulonglong, I]
+    l.gemm_testing_set_hooks.restype = I
     return l
 
 
@@ -248,6 +250,10 @@ def _host_roundtrip(fn, A, B, C, dtype_out):
     for s in streams:
         cur.wait_stream(s)
     cur.synchronize()
+    # Every chunk's GEMM is ordered before this point of `cur`: a kernel that
+    # gave up on a bounded wait left its rows of C undefined.
+    st, detail = device_status(cur)
+    _check(st, f"host-buffer GEMM (device status word {detail:#x})")
     return C
 
 
@@ -259,7 +265,13 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     (default: torch's current stream).  CPU tensors are copied to the current
     device, computed and copied back, with the copies of row chunks
     overlapping the GEMMs of others (see _host_roundtrip); the call returns
-    once C is on the host.
+    once C is on the host, after the device status word has been checked
+    (GemmError on a kernel timeout).
+
+    The device path returns as soon as the kernel is enqueued.  Its C is known
+    good only once device_status() has returned status 0 for a point after
+    the call: a kernel that gave up on a bounded wait leaves C undefined and
+    records GEMM_ERR_TIMEOUT in the device's status word instead.
     """
     import torch
     dev = _operand_device(A, B, C, stream)
@@ -300,7 +312,9 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
 
     fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
     the MMAs read; block_m: 128 or 256 rows per CTA tile, 0 to let the
-    library choose.  Every fill and tile gives the same bits."""
+    library choose.  Every fill and tile gives the same bits.  Host tensors
+    and the device status word are handled as in gemm_f32: on the device
+    path, check device_status() before trusting C."""
     import torch
     dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
@@ -338,7 +352,11 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
 
 
 def device_status(stream=None):
-    """(status, detail word) after synchronising `stream`; clears the word."""
+    """(status, detail word) after synchronising `stream`; clears the word.
+
+    The word is one per device, shared by all streams: it covers the work
+    ordered before this point of `stream`, and a kernel on another stream can
+    record (or have its record cleared) concurrently."""
     detail = ctypes.c_uint(0)
     st = lib().gemm_device_status(_stream_handle(stream), ctypes.byref(detail))
     return st, detail.value
@@ -346,3 +364,10 @@ def device_status(stream=None):
 
 def selftest_bounded_wait(timeout_us: int, stream=None) -> int:
     return lib().gemm_selftest_bounded_wait(int(timeout_us), _stream_handle(stream))
+
+
+def testing_set_hooks(wait_limit_ns: int = 0, withhold: int = -1) -> None:
+    """Test hooks (include/pipelined_gemm_testing.h): the GEMM kernels' wait
+    limit (0: the default 2 s) and a ring position their producers leave
+    unfilled (-1: none), for every later call in this process."""
+    _check(lib().gemm_testing_set_hooks(int(wait_limit_ns), int(withhold)), "gemm_testing_set_hooks")

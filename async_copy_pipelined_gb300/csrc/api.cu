@@ -13,12 +13,12 @@
 #include <cudaTypedefs.h>
 
 #include "gemm_internal.h"
+#include "pipelined_gemm_testing.h"
 #include "ptx.cuh"
 #include "tma_ring.cuh"
 
 namespace pg {
 
-constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull; // 2 s
 // Four stages for every FP32 ring fill.  Measured on GB300 (TFLOP/s, 3 / 4
 // stages, 128x128 tile at 4096^3): cp.async 55.8 / 56.0, cp.async +
@@ -55,8 +55,43 @@ __device__ unsigned int g_status_word;
 
 // ------------------------------------------------------------ device state
 static std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 ok, 2 wrong arch
-static std::atomic<uintptr_t> g_status_ptr[kMaxDevices];
 static std::atomic<int> g_num_sms[kMaxDevices];
+
+// Test hooks (pipelined_gemm_testing.h): a shorter wait limit and a ring
+// position the producers leave unfilled.  Read once per call.
+static std::atomic<unsigned long long> g_hook_wait_limit_ns{0}; // 0: kDefaultWaitLimitNs
+static std::atomic<int> g_hook_withhold{-1};
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
+// if the driver cannot say.  Per-context state (the status word's address,
+// raised shared-memory limits) is keyed on it, so a context created after
+// cudaDeviceReset starts afresh.
+static unsigned long long current_context_id()
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static std::atomic<void *> get_current{nullptr};
+    static std::atomic<void *> get_id{nullptr};
+    void *gc = get_current.load(), *gi = get_id.load();
+    if (!gc || !gi) {
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &gc, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &gi, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        get_current.store(gc);
+        get_id.store(gi);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (reinterpret_cast<GetCurrentFn>(gc)(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        reinterpret_cast<GetIdFn>(gi)(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 static int current_device(int *dev)
 {
@@ -89,18 +124,35 @@ static int check_device(int *dev_out)
     return GEMM_OK;
 }
 
-// Address of this library's status word on device `dev` (the current one).
-static unsigned int *status_word(int dev)
+// Address of this library's status word in the current context of device
+// `dev`.  Looked up once per context (`ctx` from current_context_id()); with
+// no context id it is looked up on every call.
+static unsigned int *status_word(int dev, unsigned long long ctx)
 {
-    uintptr_t p = g_status_ptr[dev].load();
-    if (p == 0) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess)
-            return nullptr;
-        p = reinterpret_cast<uintptr_t>(addr);
-        g_status_ptr[dev].store(p);
+    struct Cached {
+        std::atomic<unsigned long long> ctx{0};
+        std::atomic<uintptr_t> addr{0};
+    };
+    static Cached cache[kMaxDevices];
+    if (ctx != 0 && cache[dev].ctx.load(std::memory_order_acquire) == ctx) {
+        const uintptr_t p = cache[dev].addr.load(std::memory_order_relaxed);
+        if (p != 0)
+            return reinterpret_cast<unsigned int *>(p);
     }
-    return reinterpret_cast<unsigned int *>(p);
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess)
+        return nullptr;
+    if (ctx != 0) {
+        cache[dev].addr.store(reinterpret_cast<uintptr_t>(addr), std::memory_order_relaxed);
+        cache[dev].ctx.store(ctx, std::memory_order_release);
+    }
+    return static_cast<unsigned int *>(addr);
+}
+
+static unsigned long long hook_wait_limit_ns()
+{
+    const unsigned long long v = g_hook_wait_limit_ns.load();
+    return v != 0 ? v : kDefaultWaitLimitNs;
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -272,7 +324,10 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         args->stages = stages;
         args->tile = tile;
         args->status = nullptr;
-        args->wait_limit_ns = kDefaultWaitLimitNs;
+        args->wait_limit_ns = hook_wait_limit_ns();
+        args->withhold = g_hook_withhold.load();
+        args->device = 0;
+        args->ctx = 0;
     }
     return GEMM_OK;
 }
@@ -349,8 +404,11 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         args->block_m = block_m;
         args->c_tma = aligned16(C) && (ldc % 4) == 0 ? 1 : 0;
         args->status = nullptr;
-        args->wait_limit_ns = kDefaultWaitLimitNs;
+        args->wait_limit_ns = hook_wait_limit_ns();
+        args->withhold = g_hook_withhold.load();
         args->num_sms = 0;
+        args->device = 0;
+        args->ctx = 0;
     }
     return GEMM_OK;
 }
@@ -422,7 +480,9 @@ int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int l
         return st;
     if (M == 0 || N == 0)
         return GEMM_OK;
-    args.status = status_word(dev);
+    args.device = dev;
+    args.ctx = current_context_id();
+    args.status = status_word(dev, args.ctx);
     if (!args.status)
         return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -457,7 +517,9 @@ int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B
         return st;
     if (M == 0 || N == 0)
         return GEMM_OK;
-    args.status = status_word(dev);
+    args.device = dev;
+    args.ctx = current_context_id();
+    args.status = status_word(dev, args.ctx);
     if (!args.status)
         return GEMM_ERR_CUDA;
     args.num_sms = g_num_sms[dev].load();
@@ -473,7 +535,7 @@ int gemm_device_status(void *stream, unsigned int *detail)
     if (current_device(&dev) != GEMM_OK)
         return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned int *word = status_word(dev);
+    unsigned int *word = status_word(dev, current_context_id());
     if (!word)
         return GEMM_ERR_CUDA;
     unsigned int value = 0;
@@ -493,11 +555,20 @@ int gemm_selftest_bounded_wait(int timeout_us, void *stream)
     int st = check_device(&dev);
     if (st != GEMM_OK)
         return st;
-    unsigned int *word = status_word(dev);
+    unsigned int *word = status_word(dev, current_context_id());
     if (!word)
         return GEMM_ERR_CUDA;
     return launch_selftest_wait(word, static_cast<unsigned long long>(timeout_us) * 1000ull,
                                 static_cast<cudaStream_t>(stream));
+}
+
+int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position)
+{
+    if (withhold_position < -1 || (wait_limit_ns != 0 && wait_limit_ns < 1000000ull))
+        return GEMM_ERR_INVALID_ARG;
+    g_hook_wait_limit_ns.store(wait_limit_ns);
+    g_hook_withhold.store(withhold_position);
+    return GEMM_OK;
 }
 
 } // extern "C"

@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                 int mb, nb;
                 tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
                 for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                    if (f == p.withhold)
+                        continue; // test hook: this position is never filled
                     if (!ring.producer_acquire(f, p.wait_limit_ns)) {
                         record_error(p.status, kErrFamilyBf16 | kErrRoleProducer);
                         ok = false;
@@ -284,12 +286,14 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                                     nb * BN + j * static_cast<int>(kBBoxCols), kb * BK);
                 }
             }
-            for (int g = f > S ? f - S : 0; g < f; ++g) {
-                if (!ring.consumer_wait(g, p.wait_limit_ns)) {
-                    record_error(p.status, kErrFamilyBf16 | kErrRoleDrain);
-                    break;
-                }
-            }
+            // Only the last S positions issued can still be in flight; each
+            // is waited for, with its own bound, even after another expired.
+            bool drained = true;
+            for (int g = f > S ? f - S : 0; g < f; ++g)
+                if (g != p.withhold && !ring.consumer_wait(g, p.wait_limit_ns))
+                    drained = false;
+            if (!drained)
+                record_error(p.status, kErrFamilyBf16 | kErrRoleDrain);
         }
     } else if (Fill != GEMM_FILL_TMA && warp < R::kProducerWarps) {
         // ------------------------------------------- cp.async / sync producers
@@ -335,16 +339,22 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                     break;
                 }
                 const uint32_t dst = base + static_cast<uint32_t>(f % S) * T::kStageBytes;
+                // Test hook: position p.withhold gets no copies and no
+                // arrival, so whoever waits for it must give up.
+                const bool fill_it = f != p.withhold;
                 if constexpr (Fill == GEMM_FILL_CPASYNC) {
                     if (tile_interior && (kb + 1) * BK <= p.K) {
                         // Every chunk is a whole in-range 16-byte copy (the
                         // planner requires 16-byte row pitches).
+                        if (fill_it) {
 #pragma unroll
-                        for (int i = 0; i < kChunksPerThread; ++i) {
-                            cp_async_cg16_full(dst + c_off[i], c_src[i]);
-                            c_src[i] += c_step[i];
+                            for (int i = 0; i < kChunksPerThread; ++i)
+                                cp_async_cg16_full(dst + c_off[i], c_src[i]);
                         }
-                    } else {
+#pragma unroll
+                        for (int i = 0; i < kChunksPerThread; ++i)
+                            c_src[i] += c_step[i];
+                    } else if (fill_it) {
                         for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
                             int grow, gcol;
                             bool is_a;
@@ -366,24 +376,28 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                     if (f >= kLag) {
                         cp_async_wait<kLag>(); // this thread's copies of stage f - kLag have landed
                         fence_proxy_async_smem();
-                        mbar_arrive(ring.full_bar(f - kLag));
+                        if (f - kLag != p.withhold)
+                            mbar_arrive(ring.full_bar(f - kLag));
                     }
                 } else if (tile_interior && (kb + 1) * BK <= p.K) {
                     // Interior: every chunk of this thread loaded at once, then stored.
-                    uint4 v[kChunksPerThread];
+                    if (fill_it) {
+                        uint4 v[kChunksPerThread];
 #pragma unroll
-                    for (int i = 0; i < kChunksPerThread; ++i) {
-                        v[i] = *reinterpret_cast<const uint4 *>(c_src[i]);
-                        c_src[i] += c_step[i];
+                        for (int i = 0; i < kChunksPerThread; ++i)
+                            v[i] = *reinterpret_cast<const uint4 *>(c_src[i]);
+#pragma unroll
+                        for (int i = 0; i < kChunksPerThread; ++i)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst + c_off[i]),
+                                         "r"(v[i].x), "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                                         : "memory");
+                        fence_proxy_async_smem();
+                        mbar_arrive(ring.full_bar(f));
                     }
 #pragma unroll
                     for (int i = 0; i < kChunksPerThread; ++i)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst + c_off[i]), "r"(v[i].x),
-                                     "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
-                                     : "memory");
-                    fence_proxy_async_smem();
-                    mbar_arrive(ring.full_bar(f));
-                } else {
+                        c_src[i] += c_step[i];
+                } else if (fill_it) {
                     // Each batch keeps kBatch chunk loads per thread in flight;
                     // the batches tile the stage exactly (no chunk index past it).
                     constexpr int kBatch = 32 / R::kProducerWarps;
@@ -416,7 +430,8 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
             if (ok) {
                 fence_proxy_async_smem();
                 for (int g = f - kLag > 0 ? f - kLag : 0; g < f; ++g)
-                    mbar_arrive(ring.full_bar(g));
+                    if (g != p.withhold)
+                        mbar_arrive(ring.full_bar(g));
             }
         }
     } else if (warp == R::kMmaWarp) {
@@ -587,8 +602,8 @@ static int launch_bf16_t(const Bf16Args &a, cudaStream_t s)
         std::memset(&map_c, 0, sizeof map_c);
     }
     const int smem = bf16_smem_bytes(S, T::BM);
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<Fill, S, MH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    static std::atomic<unsigned long long> limit_set[kMaxDevices];
+    if (ensure_smem_limit(gemm_bf16_tc_kernel<Fill, S, MH>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const long long tiles = static_cast<long long>((a.M + T::BM - 1) / T::BM) * ((a.N + BN - 1) / BN);
     const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);

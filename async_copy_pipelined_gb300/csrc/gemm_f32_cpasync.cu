@@ -75,8 +75,8 @@ template <class T, int S>
 static int launch_cpasync_t(const F32Args &a, cudaStream_t s)
 {
     const int smem = S * T::kStageBytes;
-    if (cudaFuncSetAttribute(gemm_f32_cpasync_kernel<T, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    static std::atomic<unsigned long long> limit_set[kMaxDevices];
+    if (ensure_smem_limit(gemm_f32_cpasync_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
     gemm_f32_cpasync_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
     auto empty_bar = [&](int f) { return empty0 + 8u * static_cast<uint32_t>(f % S); };
     auto parity = [](int f) { return static_cast<uint32_t>((f / S) & 1); };
     auto issue = [&](int f) {
+        if (f == p.withhold)
+            return; // test hook: no copies and no arrival for this position
         issue_slice_cpasync<T>(stage0 + (f % S) * T::kStageFloats, p, tid, m0, n0, f);
         cp_async_mbar_arrive_noinc(full_bar(f));
     };
@@ -136,8 +138,8 @@ template <class T, int S>
 static int launch_cpasync_mbar_t(const F32Args &a, cudaStream_t s)
 {
     const int smem = f32_smem_bytes(T::BM, GEMM_FILL_CPASYNC_MBAR, S);
-    if (cudaFuncSetAttribute(gemm_f32_cpasync_mbar_kernel<T, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+    static std::atomic<unsigned long long> limit_set[kMaxDevices];
+    if (ensure_smem_limit(gemm_f32_cpasync_mbar_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
     gemm_f32_cpasync_mbar_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);

@@ -76,8 +76,8 @@ template <class T>
 static int launch_sync_t(const F32Args &a, cudaStream_t s)
 {
     const int smem = T::kStageBytes;
-    if (cudaFuncSetAttribute(gemm_f32_sync_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    static std::atomic<unsigned long long> limit_set[kMaxDevices];
+    if (ensure_smem_limit(gemm_f32_sync_kernel<T>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
     gemm_f32_sync_kernel<T><<<grid, T::kThreads, smem, s>>>(a);

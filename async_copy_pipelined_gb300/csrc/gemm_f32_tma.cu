@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
             tma_prefetch_map(&map_b);
             int f = 0;
             for (; f < k_slices; ++f) {
+                if (f == p.withhold)
+                    continue; // test hook: this position is never filled
                 if (!ring.producer_acquire(f, p.wait_limit_ns)) {
                     record_error(p.status, kErrFamilyF32Tma | kErrRoleProducer);
                     break;
@@ -68,13 +70,17 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
                 tma_load_2d(dst, &map_a, ring.full_bar(f), f * T::BK, m0);
                 tma_load_2d(dst + T::kAFloats * 4, &map_b, ring.full_bar(f), n0, f * T::BK);
             }
-            // Copies still in flight must land before the CTA exits.
-            for (int g = f > S ? f - S : 0; g < f; ++g) {
-                if (!ring.consumer_wait(g, p.wait_limit_ns)) {
-                    record_error(p.status, kErrFamilyF32Tma | kErrRoleDrain);
-                    break;
-                }
-            }
+            // Copies still in flight must land before the CTA exits: only
+            // the last S positions issued can still be in flight (issuing
+            // position g + S waited for g's release, which followed its
+            // landing).  Each is waited for, with its own bound, even after
+            // another has expired.
+            bool drained = true;
+            for (int g = f > S ? f - S : 0; g < f; ++g)
+                if (g != p.withhold && !ring.consumer_wait(g, p.wait_limit_ns))
+                    drained = false;
+            if (!drained)
+                record_error(p.status, kErrFamilyF32Tma | kErrRoleDrain);
         }
         return;
     }
@@ -139,8 +145,8 @@ static int launch_tma_t(const F32Args &a, cudaStream_t s)
     if (st != GEMM_OK)
         return st;
     const int smem = f32_smem_bytes(T::BM, GEMM_FILL_TMA, S);
-    if (cudaFuncSetAttribute(gemm_f32_tma_kernel<T, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    static std::atomic<unsigned long long> limit_set[kMaxDevices];
+    if (ensure_smem_limit(gemm_f32_tma_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
     gemm_f32_tma_kernel<T, S><<<grid, tma_threads<T>(), smem, s>>>(map_a, map_b, a);

@@ -2,6 +2,7 @@
 // translation units.  Not installed; not part of the public header.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -25,6 +26,9 @@ struct F32Args {
     int tile; // 64 or 128
     unsigned int *status; // device status word
     unsigned long long wait_limit_ns;
+    int withhold;          // ring position a producer leaves unfilled (test hook; -1: none)
+    int device;            // current device index
+    unsigned long long ctx; // unique id of the current context (0: unknown)
 };
 
 struct Bf16Args {
@@ -40,8 +44,29 @@ struct Bf16Args {
     int c_tma;    // 1: C is written by TMA stores (16-byte aligned C, ldc % 4 == 0)
     unsigned int *status;
     unsigned long long wait_limit_ns;
+    int withhold; // ring position the producers leave unfilled (test hook; -1: none)
     int num_sms;
+    int device;
+    unsigned long long ctx;
 };
+
+constexpr int kMaxDevices = 64;
+
+// Raise a kernel's dynamic shared-memory limit once per context rather than
+// on every launch: `done[dev]` holds the id of the context in which it was
+// last raised, so a context created after cudaDeviceReset raises it again.
+template <class Kernel>
+int ensure_smem_limit(Kernel kernel, int smem, int dev, unsigned long long ctx,
+                      std::atomic<unsigned long long> (&done)[kMaxDevices])
+{
+    if (ctx != 0 && dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire) == ctx)
+        return GEMM_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (ctx != 0 && dev >= 0 && dev < kMaxDevices)
+        done[dev].store(ctx, std::memory_order_release);
+    return GEMM_OK;
+}
 
 // Launchers: each returns a gemm_status.  They assume validated arguments.
 int launch_f32_sync(const F32Args &a, cudaStream_t s);

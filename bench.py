@@ -41,7 +41,14 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOP/s and % of FP32-FFMA / BF16-tensor peak, pipelined vs sync fill"
 UNIT = "TFLOP/s"
 FP32_FMA_PER_SM_PER_CLK = 128        # FP32 lanes per SM on sm_100-family parts
-NOMINAL_BF16_DENSE_TFLOPS = 2250.0   # GB300 dense BF16, without 2:4 sparsity
+# Dense BF16 tensor-core work per SM per clock on sm_100-family parts
+# (tcgen05.mma kind::f16, no 2:4 sparsity): twice Hopper's.  Hopper's figure
+# follows from NVIDIA's H100 SXM5 datasheet: 989.4 dense BF16 TFLOP/s at the
+# 1830 MHz boost clock on 132 SMs = 4096 FLOP per SM per clock; NVIDIA's
+# Blackwell material states the fifth-generation tensor core doubles the
+# per-SM FP16/BF16 rate.  bench.py also measures it (tensor_rate_probe) when
+# the library provides the probe.
+BF16_DENSE_FLOP_PER_SM_PER_CLK = 8192
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 256 << 20              # > 2x the 126 MiB L2
@@ -167,6 +174,47 @@ def fp32_peak_tflops(num_sms: int, mhz: float) -> float:
     return num_sms * FP32_FMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
 
 
+def bf16_derived_peak_tflops(num_sms: int, mhz: float, per_sm_per_clk: float = BF16_DENSE_FLOP_PER_SM_PER_CLK) -> float:
+    return num_sms * per_sm_per_clk * mhz * 1e6 / 1e12
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = {}
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+        for key in ("model name", "hardware", "cpu part"):
+            if key in fields:
+                return fields[key] if key != "cpu part" else f"CPU part {fields[key]}"
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class DeviceStatusError(RuntimeError):
+    pass
+
+
+def check_status(pg, what: str):
+    """A kernel that gave up on a bounded wait leaves C undefined: its timing
+    is not a measurement of the GEMM."""
+    st, detail = pg.device_status()
+    if st != 0:
+        raise DeviceStatusError(f"device status {st} ({detail:#x}) after {what}")
+
+
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
@@ -186,9 +234,12 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            import atexit
+            atexit.register(self.stop)  # never leave the sampler running past an early exit
 
     def stop(self):
-        if self.proc is None:
+        if self.proc is None or self.proc.returncode is not None:
             return
         self.proc.terminate()
         try:
@@ -329,8 +380,29 @@ def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
         call()
         timer.end()
     torch.cuda.synchronize()
+    check_status(pg, "a timed side leg")
     d = timer.durations_ms()
     return statistics.mean(d), min(d), statistics.median(d)
+
+
+def clocks_during(call, seconds: float, uuid):
+    """Median SM clock (nvidia-smi samples) while `call` runs back to back
+    for about `seconds`."""
+    import torch
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_end = time.perf_counter() + seconds
+    launches = 0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            call()
+        launches += 50
+        torch.cuda.synchronize()
+    sampler.stop()
+    out = sampler.summary()
+    out["launches"] = launches
+    return out
 
 
 # --------------------------------------------------------------------- oracle leg
@@ -354,7 +426,7 @@ def oracle_sample(name: str, A, B, w, seconds: float, gpu_rows=None):
     t = time.perf_counter() - t0
     res = {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
            "sample": f"first {rows} of {M} output rows (all {N} columns, K={K}); {t:.2f} s on the host cores",
-           "seconds": t, "rows": rows}
+           "seconds": t, "rows": rows, "cpu_model": host_cpu_model(), "nproc": os.cpu_count()}
     if gpu_rows is not None:
         g = gpu_rows[:rows].astype(np.float64)
         res["max_abs_diff_vs_gpu"] = float(np.max(np.abs(g - out)))
@@ -428,7 +500,8 @@ def run_reference(args, dist: Dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64" if not name.startswith("bf16") else "f64 (bf16 inputs)", "data": "synthetic",
         "config": workload_config(name, w, None),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": host_cpu_model(), "nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -524,6 +597,11 @@ def run_ours(args, dist: Dist):
 
     timer = CudaTimer()
     total_ms, per = timed_loop(dist, args.steps, args.warmup, call, flush, timer, torch.cuda.synchronize)
+    st, detail = pg.device_status()
+    if st != 0:
+        sampler.stop()
+        print(json.dumps({"error": f"device status {st} ({detail:#x}) after the timed loop"}), flush=True)
+        return 1
     launches = args.steps
     ms_step = total_ms / args.steps
     value = dist.world * flops * args.steps / (total_ms / 1e3) / 1e12
@@ -614,9 +692,23 @@ def run_ours(args, dist: Dist):
                 hbm_b = float(peaks.get("hbm_gbs") or 0.0)
                 roof_b["dram_gbs"] = roof_b["traffic"] / (mean / 1e3) / 1e9
                 roof_b["dram_frac_of_hbm"] = roof_b["dram_gbs"] / hbm_b if hbm_b else None
+            # The chip's dense BF16 peak derived from SM count x per-SM rate x
+            # clock, at the maximum SM clock and at the clock sampled while
+            # this kernel runs back to back (the tensor cores draw enough power
+            # to lower it).
+            bclk = clocks_during(cb, 1.0, sampler.uuid)
+            launches += bclk.pop("launches", 0)
+            check_status(pg, "the BF16 clock sample")
+            derived = {"per_sm_per_clk": BF16_DENSE_FLOP_PER_SM_PER_CLK, "sms": num_sms,
+                       "at_max_clock": {"mhz": sm_max, "tflops": bf16_derived_peak_tflops(num_sms, sm_max)},
+                       "clocks_while_running": bclk}
+            derived["at_max_clock"]["frac"] = tf / derived["at_max_clock"]["tflops"]
+            if bclk.get("sm_mhz"):
+                p_obs = bf16_derived_peak_tflops(num_sms, bclk["sm_mhz"])
+                derived["at_sampled_clock"] = {"mhz": bclk["sm_mhz"], "tflops": p_obs, "frac": tf / p_obs}
             extras["bf16_8192"] = {"tflops": tf, "ms": mean, "ms_min": best, "ms_median": med,
                                    "stages": pb["stages"], "block_m": pb["block_m"], "roofline": roof_b,
-                                   "frac_nominal_dense_2250": tf / NOMINAL_BF16_DENSE_TFLOPS}
+                                   "derived_peak": derived}
             bfills = {}
             for f, s, t in (("tma", 2, 128), ("tma", 3, 128), ("tma", 4, 128), ("cpasync", 2, 128),
                             ("cpasync", 4, 128), ("sync", 1, 128), ("tma", 2, 256), ("tma", 3, 256),
@@ -666,7 +758,12 @@ def run_ours(args, dist: Dist):
     if is_bf16:
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": UNIT,
                 "frac": achieved / bf16_peak, "traffic": profiled_traffic(kernel_key),
-                "peak_source": f"{peaks['_source']} (MEASURED_PEAKS bf16_tflops, cuBLAS burst)"}
+                "peak_source": f"{peaks['_source']} (MEASURED_PEAKS bf16_tflops, cuBLAS burst)",
+                "derived_peak_at_max_clock": bf16_derived_peak_tflops(num_sms, sm_max),
+                "frac_of_derived_peak_at_max_clock": achieved / bf16_derived_peak_tflops(num_sms, sm_max)}
+        if clocks.get("sm_mhz"):
+            roof["frac_of_derived_peak_at_observed_clock"] = achieved / bf16_derived_peak_tflops(num_sms,
+                                                                                                 clocks["sm_mhz"])
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": UNIT,
                 "frac": achieved / fp32_peak, "traffic": profiled_traffic(kernel_key),
@@ -749,6 +846,9 @@ def main(argv=None):
     dist = Dist()
     try:
         return run_ours(args, dist)
+    except DeviceStatusError as e:
+        print(json.dumps({"error": str(e)}), flush=True)
+        return 1
     finally:
         dist.close()
 

@@ -53,8 +53,10 @@
  * Errors: a status code is returned; nothing is enqueued unless the status
  * is GEMM_OK.  The library never exits the process and never falls back
  * silently from one fill to another.  A kernel whose internal wait exceeds
- * its time limit records GEMM_ERR_TIMEOUT in a device status word, which
- * gemm_device_status() reads.
+ * its time limit (2 s) records GEMM_ERR_TIMEOUT in a device status word,
+ * which gemm_device_status() reads: a caller of the device path checks it
+ * before trusting C.  Test hooks that make those waits expire on purpose are
+ * declared in pipelined_gemm_testing.h.
  */
 #ifndef PIPELINED_GEMM_H
 #define PIPELINED_GEMM_H
@@ -218,7 +220,23 @@ const char *gemm_status_string(int status);
  * GEMM_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
  * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async),
- * bits 8-15 the waiting role.
+ * bits 8-15 the waiting role (1 consumer, 2 producer, 3 MMA issuer,
+ * 4 epilogue, 5 drain of copies or MMAs still in flight).
+ *
+ * The word is ONE per device (per CUDA context), shared by every call on
+ * every stream and every host thread.  A kernel records only the first
+ * expiry after the last clear.  Consequences:
+ *   - the synchronisation covers only work ordered before this point of
+ *     `stream`; a kernel on another stream that has not finished yet may
+ *     still record an expiry after the read;
+ *   - the read and the clear are two separate steps, so an expiry recorded
+ *     between them by a kernel on another stream is lost, and calls that
+ *     overlap on the GPU race on the word: whichever caller reads first
+ *     sees (and clears) the other's error.
+ * Callers that need a per-call verdict serialise their GEMMs on one stream
+ * and call gemm_device_status after each.  GEMM results on the device path
+ * are only known good once gemm_device_status has returned GEMM_OK for a
+ * point after them.
  */
 int gemm_device_status(void *stream, unsigned int *detail);
 

@@ -1,0 +1,50 @@
+/*
+ * pipelined_gemm_testing.h -- test hooks of the pipelined GEMM library.
+ *
+ * Not for production use.  The hooks exist so that a test can make the GEMM
+ * kernels' own bounded waits expire, and check that each kernel gives up,
+ * reports GEMM_ERR_TIMEOUT, waits for its own copies and tensor-core work
+ * still in flight, frees its tensor memory and returns, leaving the CUDA
+ * context usable.  No GPU is faulted, trapped or hung to do so: a producer
+ * simply never fills one ring position, the way a partial commit would
+ * strand the block ("Day 74: Async copies and pipelines", section
+ * "Pitfalls": a missing commit or arrival leaves the waiting threads
+ * waiting forever), and every wait on that position runs into its limit.
+ */
+#ifndef PIPELINED_GEMM_TESTING_H
+#define PIPELINED_GEMM_TESTING_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * gemm_testing_set_hooks: process-wide settings that every later gemm_f32 /
+ * gemm_bf16 call reads when it is made (calls already enqueued keep theirs).
+ *
+ *   wait_limit_ns      limit of every bounded wait in the GEMM kernels, in
+ *                      nanoseconds; 0 restores the default of 2 s.  Values
+ *                      below 1 ms are refused.
+ *   withhold_position  ring position (0, 1, 2, ... counted per CTA over all
+ *                      of its K slices, and over its tiles for the
+ *                      persistent tensor-core kernel) that the producers of
+ *                      the FP32 TMA fill, the FP32 mbarrier-completed
+ *                      cp.async fill and all three BF16 fills leave
+ *                      unfilled: no copy is issued and no arrival (and, for
+ *                      TMA, no expected-transaction count) is made for it.
+ *                      -1 restores normal operation.  The FP32 sync and
+ *                      group-completed cp.async fills have no waits and
+ *                      ignore it.
+ *
+ * With a position withheld, the C output of a call is undefined and the call
+ * ends with GEMM_ERR_TIMEOUT in the status word (gemm_device_status).
+ * Returns GEMM_OK or GEMM_ERR_INVALID_ARG.  Not thread-safe against
+ * concurrent GEMM calls that expect the defaults.
+ */
+int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIPELINED_GEMM_TESTING_H */

@@ -204,3 +204,14 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         mod.lib()
+
+
+def test_testing_hooks_validate_and_reset(lib):
+    """The test hooks are host-side settings: limits below 1 ms and
+    positions below -1 are refused, and the defaults can always be restored
+    (no device is touched)."""
+    assert lib.gemm_testing_set_hooks(999_999, -1) == 1
+    assert lib.gemm_testing_set_hooks(0, -2) == 1
+    assert lib.gemm_testing_set_hooks(10_000_000, 3) == 0
+    assert lib.gemm_testing_set_hooks(0, -1) == 0
+    assert "gemm_testing_set_hooks" in _declared_functions()
