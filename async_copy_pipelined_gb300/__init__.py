@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = [
-    "FILL", "GemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "plan_f32", "plan_bf16",
+    "FILL", "OPTIONS", "GemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "plan_f32", "plan_bf16",
     "device_status", "selftest_bounded_wait", "testing_set_hooks", "status_string", "build",
 ]
 
@@ -28,6 +28,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libpipelined_gemm.so")
 
 FILL = {"sync": 0, "cpasync": 1, "tma": 2, "cpasync_mbar": 3}
+# Cache-qualifier options (include/pipelined_gemm.h, GEMM_OPT_*), OR-ed into
+# the fill code: pass e.g. fill="cpasync", options=("l2_prefetch_128b",).
+OPTIONS = {"l2_prefetch_128b": 0x100, "a_evict_first": 0x200, "a_evict_last": 0x400, "b_evict_first": 0x800,
+           "b_evict_last": 0x1000}
 
 GEMM_OK = 0
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_UNSUPPORTED",
@@ -46,7 +50,8 @@ class GemmError(RuntimeError):
 class GemmPlan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "fill_mode", "block_m", "block_n", "block_k", "thread_m", "thread_n", "threads", "stages",
-        "a_copy_bytes", "b_copy_bytes", "smem_bytes", "grid_x", "grid_y", "k_slices")]
+        "a_copy_bytes", "b_copy_bytes", "smem_bytes", "grid_x", "grid_y", "k_slices", "options",
+        "persistent_ctas", "workspace_bytes")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -65,6 +70,8 @@ def _bind(l):
     I, P, U = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint)
     l.gemm_f32.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]
     l.gemm_f32.restype = I
+    l.gemm_f32_ws.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P]
+    l.gemm_f32_ws.restype = I
     l.gemm_f32_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, ctypes.POINTER(GemmPlan)]
     l.gemm_f32_plan.restype = I
     l.gemm_bf16.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]
@@ -81,6 +88,10 @@ def _bind(l):
     l.gemm_version.restype = I
     l.gemm_testing_set_hooks.argtypes = [ctypes.c_ulonglong, I]
     l.gemm_testing_set_hooks.restype = I
+    l.gemm_testing_withhold_handover.argtypes = [I]
+    l.gemm_testing_withhold_handover.restype = I
+    l.gemm_testing_f32_piece.argtypes = [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)]
+    l.gemm_testing_f32_piece.restype = I
     return l
 
 
@@ -111,12 +122,18 @@ def _stream_handle(stream):
     return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _fill_code(fill) -> int:
+def _fill_code(fill, options=()) -> int:
     if isinstance(fill, str):
         if fill not in FILL:
             raise ValueError(f"fill must be one of {sorted(FILL)}")
-        return FILL[fill]
-    return int(fill)
+        code = FILL[fill]
+    else:
+        code = int(fill)
+    for o in options:
+        if o not in OPTIONS:
+            raise ValueError(f"options must be among {sorted(OPTIONS)}")
+        code |= OPTIONS[o]
+    return code
 
 
 def _matrix_args(x, name):
@@ -169,20 +186,20 @@ def _check(status: int, what: str):
 
 
 def plan_f32(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_tile=0,
-             a_ptr=256, b_ptr=256, c_ptr=256) -> dict:
+             a_ptr=256, b_ptr=256, c_ptr=256, options=()) -> dict:
     """What gemm_f32 would launch for these sizes (no device access)."""
     p = GemmPlan()
     st = lib().gemm_f32_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
-                             _fill_code(fill), stages, block_tile, ctypes.byref(p))
+                             _fill_code(fill, options), stages, block_tile, ctypes.byref(p))
     _check(st, "gemm_f32_plan")
     return p.as_dict()
 
 
 def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block_m=0, a_ptr=256, b_ptr=256,
-              c_ptr=256) -> dict:
+              c_ptr=256, options=()) -> dict:
     p = GemmPlan()
     st = lib().gemm_bf16_plan(M, N, K, a_ptr, lda or max(K, 1), b_ptr, ldb or max(N, 1), c_ptr, ldc or max(N, 1),
-                              _fill_code(fill), stages, block_m, ctypes.byref(p))
+                              _fill_code(fill, options), stages, block_m, ctypes.byref(p))
     _check(st, "gemm_bf16_plan")
     return p.as_dict()
 
@@ -257,7 +274,21 @@ def _host_roundtrip(fn, A, B, C, dtype_out):
     return C
 
 
-def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
+# Hand-over workspaces of gemm_f32_ws, one per (device, stream): a workspace
+# serves one call at a time, and calls on one stream never overlap.
+_workspaces = {}
+
+
+def _workspace(dev, stream_handle: int, nbytes: int):
+    import torch
+    key = (dev.index, stream_handle)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = _workspaces[key] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    return buf
+
+
+def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, options=(), workspace="auto"):
     """C = A @ B in float32 through the library's FP32 kernel with the given fill.
 
     A (M x K), B (K x N) float32 tensors; C (M x N) float32 output, allocated
@@ -267,6 +298,16 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     overlapping the GEMMs of others (see _host_roundtrip); the call returns
     once C is on the host, after the device status word has been checked
     (GemmError on a kernel timeout).
+
+    options: cache-qualifier names from OPTIONS (GEMM_OPT_* in the C
+    header): an L2 prefetch size for cp.async copies and L2 eviction
+    priorities for A and B; none changes a result bit.
+
+    workspace: hand-over space for the persistent TMA kernel's split of the
+    last round of tiles (gemm_f32_ws in the C header).  "auto" keeps one
+    buffer per device and stream, grown as needed; None runs without the
+    split; a uint8 CUDA tensor is used as given.  The bits are the same
+    either way.
 
     The device path returns as soon as the kernel is enqueued.  Its C is known
     good only once device_status() has returned status 0 for a point after
@@ -286,7 +327,8 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
             except (RuntimeError, ValueError):
                 pass  # the chunk calls report the error
         return _host_roundtrip(lambda a, b, s: gemm_f32(a, b, None, fill=fill, stages=stages,
-                                                        block_tile=block_tile, stream=s),
+                                                        block_tile=block_tile, stream=s, options=options,
+                                                        workspace=workspace),
                                A, B, C, torch.float32)
     if A.dtype != torch.float32 or B.dtype != torch.float32:
         raise TypeError("gemm_f32 takes float32 tensors")
@@ -300,14 +342,25 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None):
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
     _refuse_aliased_output(C, A, B)
+    code = _fill_code(fill, options)
     with torch.cuda.device(dev):
-        st = lib().gemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_tile,
-                            _stream_handle(stream))
+        sh = _stream_handle(stream)
+        ws_ptr, ws_bytes = None, 0
+        if workspace is not None:
+            plan = GemmPlan()
+            st = lib().gemm_f32_plan(M, N, K, pa, lda, pb, ldb, pc, ldc, code, stages, block_tile, ctypes.byref(plan))
+            _check(st, "gemm_f32_plan")
+            if plan.workspace_bytes > 0:
+                ws = _workspace(dev, sh.value or 0, plan.workspace_bytes) if isinstance(workspace, str) else workspace
+                if ws.device != dev:
+                    raise ValueError(f"workspace is on {ws.device}, operands on {dev}")
+                ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+        st = lib().gemm_f32_ws(M, N, K, pa, lda, pb, ldb, pc, ldc, code, stages, block_tile, ws_ptr, ws_bytes, sh)
     _check(st, "gemm_f32")
     return C
 
 
-def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
+def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, options=()):
     """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores.
 
     fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
@@ -330,7 +383,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
             except (RuntimeError, ValueError):
                 pass  # the chunk calls report the error
         return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, block_m=block_m,
-                                                         stream=s),
+                                                         stream=s, options=options),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")
@@ -345,7 +398,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None):
         raise ValueError("C must be a float32 M x N tensor")
     _refuse_aliased_output(C, A, B)
     with torch.cuda.device(dev):
-        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill), stages, block_m,
+        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill, options), stages, block_m,
                              _stream_handle(stream))
     _check(st, "gemm_bf16")
     return C

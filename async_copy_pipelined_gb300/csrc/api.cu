@@ -7,11 +7,13 @@
 // refuse an unsuitable device before doing anything, check every result
 // before timing) but reports a status code instead of exiting.
 #include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 
 #include <cudaTypedefs.h>
 
+#include "f32_schedule.cuh"
 #include "gemm_internal.h"
 #include "pipelined_gemm_testing.h"
 #include "ptx.cuh"
@@ -61,6 +63,7 @@ static std::atomic<int> g_num_sms[kMaxDevices];
 // position the producers leave unfilled.  Read once per call.
 static std::atomic<unsigned long long> g_hook_wait_limit_ns{0}; // 0: kDefaultWaitLimitNs
 static std::atomic<int> g_hook_withhold{-1};
+static std::atomic<int> g_hook_withhold_handover{0};
 
 // Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
 // if the driver cannot say.  Per-context state (the status word's address,
@@ -149,6 +152,28 @@ static unsigned int *status_word(int dev, unsigned long long ctx)
     return static_cast<unsigned int *>(addr);
 }
 
+// Value the ready flags of the next persistent FP32 call carry: unique per
+// call within the process, and salted so that no value left in a reused
+// hand-over buffer by another process or library instance matches it.
+static unsigned long long next_epoch()
+{
+    static std::atomic<unsigned long long> counter{0};
+    unsigned long long v = counter.load();
+    if (v == 0) {
+        // SplitMix64's finaliser (Steele, Lea & Flood 2014) over the clock
+        // and an address of this instance.
+        unsigned long long z = static_cast<unsigned long long>(
+                                   std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                               reinterpret_cast<uintptr_t>(&counter);
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        z ^= z >> 31;
+        unsigned long long expected = 0;
+        counter.compare_exchange_strong(expected, z | 1ull);
+    }
+    return counter.fetch_add(1) + 1;
+}
+
 static unsigned long long hook_wait_limit_ns()
 {
     const unsigned long long v = g_hook_wait_limit_ns.load();
@@ -204,7 +229,9 @@ int f32_smem_bytes(int tile, int fill, int stages)
         return stage_bytes;
     if (fill == GEMM_FILL_CPASYNC)
         return stages * stage_bytes;
-    return stages * stage_bytes + 16 * stages + 1024; // TMA / mbarrier ring: + barriers + alignment slack
+    // TMA / mbarrier ring: + its barriers, two hand-over barriers, a flag and
+    // the work schedule (the persistent TMA kernel), and alignment slack.
+    return stages * stage_bytes + 16 * stages + 64 + 1024;
 }
 
 
@@ -242,13 +269,45 @@ static int planning_sms()
     return kPlanningSms;
 }
 
+// Split fill_mode into the fill (low byte) and the cache-qualifier options
+// (GEMM_OPT_*), and check that the options suit the fill: the prefetch size
+// is a cp.async qualifier; L2 policies go on cp.async and TMA copies, not on
+// the register path's plain loads.  Fills out the copy form and policies.
+static int decode_options(int fill_mode, int *fill, int *copy_form, int *pol_a, int *pol_b)
+{
+    const int opts = fill_mode & ~0xFF;
+    *fill = fill_mode & 0xFF;
+    *copy_form = 0;
+    *pol_a = *pol_b = 0;
+    if (opts & ~GEMM_OPT_MASK)
+        return GEMM_ERR_INVALID_ARG;
+    if ((opts & GEMM_OPT_A_EVICT_FIRST) && (opts & GEMM_OPT_A_EVICT_LAST))
+        return GEMM_ERR_INVALID_ARG;
+    if ((opts & GEMM_OPT_B_EVICT_FIRST) && (opts & GEMM_OPT_B_EVICT_LAST))
+        return GEMM_ERR_INVALID_ARG;
+    const bool cpasync = *fill == GEMM_FILL_CPASYNC || *fill == GEMM_FILL_CPASYNC_MBAR;
+    const bool policy = (opts & (GEMM_OPT_A_EVICT_FIRST | GEMM_OPT_A_EVICT_LAST | GEMM_OPT_B_EVICT_FIRST |
+                                 GEMM_OPT_B_EVICT_LAST)) != 0;
+    if ((opts & GEMM_OPT_L2_PREFETCH_128B) && !cpasync)
+        return GEMM_ERR_INVALID_ARG;
+    if (policy && !cpasync && *fill != GEMM_FILL_TMA)
+        return GEMM_ERR_INVALID_ARG;
+    *copy_form = ((opts & GEMM_OPT_L2_PREFETCH_128B) ? 1 : 0) | (policy ? 2 : 0);
+    *pol_a = (opts & GEMM_OPT_A_EVICT_FIRST) ? 1 : (opts & GEMM_OPT_A_EVICT_LAST) ? 2 : 0;
+    *pol_b = (opts & GEMM_OPT_B_EVICT_FIRST) ? 1 : (opts & GEMM_OPT_B_EVICT_LAST) ? 2 : 0;
+    return GEMM_OK;
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
-                    int fill, int stages, int tile, gemm_plan *plan, F32Args *args)
+                    int fill_mode, int stages, int tile, gemm_plan *plan, F32Args *args)
 {
     if (M < 0 || N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    int fill, copy_form, pol_a, pol_b;
+    if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
         return GEMM_ERR_INVALID_ARG;
     if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA &&
         fill != GEMM_FILL_CPASYNC_MBAR)
@@ -281,10 +340,31 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     const bool c_vec = aligned16(C) && (ldc % 4) == 0;
     if (fill == GEMM_FILL_TMA && K > 0 && work && (!a_vec || !b_vec))
         return GEMM_ERR_MISALIGNED;
+    // Rows that are not 16-byte aligned are copied 4 bytes at a time
+    // (cp.async.ca); those copies carry no cache policy.
+    if ((copy_form & 2) != 0 && (fill == GEMM_FILL_CPASYNC || fill == GEMM_FILL_CPASYNC_MBAR) && K > 0 && work &&
+        (!a_vec || !b_vec))
+        return GEMM_ERR_UNSUPPORTED;
     const long long grid_y = (M + tile - 1) / tile;
     const long long grid_x = (N + tile - 1) / tile;
     if (grid_y > 65535 || grid_x * grid_y > 0x7fffffffLL)
         return GEMM_ERR_INVALID_ARG;
+    // The TMA fill's 128 x 128 tile: with hand-over space (gemm_f32_ws) and
+    // a tile count that is not a multiple of the SM count, the last round
+    // and one more are split in K over one CTA per SM (f32_schedule.cuh).
+    int ctas = 0;
+    long long handover = 0;
+    int region0 = 0x7fffffff;
+    if (fill == GEMM_FILL_TMA && tile == 128 && work && K > 0) {
+        const long long tiles = grid_x * grid_y;
+        const int sms = planning_sms();
+        const F32Schedule sch = F32Schedule::make(static_cast<int>(tiles), sms, (K + 15) / 16, true);
+        if (sch.split()) {
+            ctas = sms;
+            handover = f32_handover_bytes(sms);
+            region0 = sch.region0;
+        }
+    }
 
     if (plan) {
         std::memset(plan, 0, sizeof *plan);
@@ -307,6 +387,9 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         plan->grid_x = static_cast<int>(grid_x);
         plan->grid_y = static_cast<int>(grid_y);
         plan->k_slices = (K + 15) / 16;
+        plan->options = fill_mode & GEMM_OPT_MASK;
+        plan->persistent_ctas = ctas;
+        plan->workspace_bytes = static_cast<int>(handover);
     }
     if (args) {
         args->M = M;
@@ -326,6 +409,17 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         args->status = nullptr;
         args->wait_limit_ns = hook_wait_limit_ns();
         args->withhold = g_hook_withhold.load();
+        args->copy_form = copy_form;
+        args->pol_a = pol_a;
+        args->pol_b = pol_b;
+        args->ctas = 0;         // set when the call brings hand-over space
+        args->tile_limit = 0x7fffffff;
+        args->split_ctas = ctas;
+        args->split_region0 = region0;
+        args->withhold_handover = g_hook_withhold_handover.load();
+        args->handover = nullptr;
+        args->handover_bytes = handover;
+        args->epoch = 0;
         args->device = 0;
         args->ctx = 0;
     }
@@ -333,9 +427,12 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
 }
 
 static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
-                     int fill, int stages, int block_m, gemm_plan *plan, Bf16Args *args)
+                     int fill_mode, int stages, int block_m, gemm_plan *plan, Bf16Args *args)
 {
     if (M < 0 || N < 0 || K < 0)
+        return GEMM_ERR_INVALID_ARG;
+    int fill, copy_form, pol_a, pol_b;
+    if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
         return GEMM_ERR_INVALID_ARG;
     if (fill == GEMM_FILL_CPASYNC_MBAR)
         return GEMM_ERR_UNSUPPORTED;
@@ -389,6 +486,10 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         plan->grid_x = static_cast<int>(tiles_m * tiles_n); // upper bound; capped at the SM count on launch
         plan->grid_y = 1;
         plan->k_slices = (K + kBf16BlockK - 1) / kBf16BlockK;
+        plan->options = fill_mode & GEMM_OPT_MASK;
+        plan->persistent_ctas = static_cast<int>(tiles_m * tiles_n < planning_sms() ? tiles_m * tiles_n
+                                                                                    : planning_sms());
+        plan->workspace_bytes = 0;
     }
     if (args) {
         args->M = M;
@@ -406,6 +507,9 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         args->status = nullptr;
         args->wait_limit_ns = hook_wait_limit_ns();
         args->withhold = g_hook_withhold.load();
+        args->copy_form = copy_form;
+        args->pol_a = pol_a;
+        args->pol_b = pol_b;
         args->num_sms = 0;
         args->device = 0;
         args->ctx = 0;
@@ -470,10 +574,26 @@ int gemm_f32_plan(int M, int N, int K, const float *A, int lda, const float *B, 
 int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc, int fill_mode,
              int stages, int block_tile, void *stream)
 {
+    return gemm_f32_ws(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_tile, nullptr, 0, stream);
+}
+
+int gemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                int fill_mode, int stages, int block_tile, void *workspace, size_t workspace_bytes, void *stream)
+{
     F32Args args;
     int st = plan_f32(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_tile, nullptr, &args);
     if (st != GEMM_OK)
         return st;
+    if (workspace != nullptr && args.handover_bytes > 0) {
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+            return GEMM_ERR_MISALIGNED;
+        if (workspace_bytes < static_cast<size_t>(args.handover_bytes))
+            return GEMM_ERR_INVALID_ARG;
+        args.handover = workspace;
+        args.epoch = next_epoch();
+        args.ctas = args.split_ctas;
+        args.tile_limit = args.split_region0;
+    }
     int dev;
     st = check_device(&dev);
     if (st != GEMM_OK)
@@ -488,7 +608,7 @@ int gemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int l
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return launch_f32_zero(args, s);
-    switch (fill_mode) {
+    switch (fill_mode & 0xFF) {
     case GEMM_FILL_SYNC: return launch_f32_sync(args, s);
     case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);
     case GEMM_FILL_CPASYNC_MBAR: return launch_f32_cpasync_mbar(args, s);
@@ -526,7 +646,7 @@ int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return launch_bf16_zero(args, s);
-    return launch_bf16(args, fill_mode, s);
+    return launch_bf16(args, fill_mode & 0xFF, s);
 }
 
 int gemm_device_status(void *stream, unsigned int *detail)
@@ -560,6 +680,28 @@ int gemm_selftest_bounded_wait(int timeout_us, void *stream)
         return GEMM_ERR_CUDA;
     return launch_selftest_wait(word, static_cast<unsigned long long>(timeout_us) * 1000ull,
                                 static_cast<cudaStream_t>(stream));
+}
+
+int gemm_testing_withhold_handover(int on)
+{
+    g_hook_withhold_handover.store(on ? 1 : 0);
+    return GEMM_OK;
+}
+
+int gemm_testing_f32_piece(int tiles, int ctas, int k_slices, int split, int cta, int idx, int *out)
+{
+    if (!out || tiles < 0 || ctas < 1 || k_slices < 1 || cta < 0 || cta >= ctas || idx < 0)
+        return 0;
+    const F32CtaPieces q = F32CtaPieces::make(F32Schedule::make(tiles, ctas, k_slices, split != 0), cta);
+    if (idx >= q.count())
+        return 0;
+    const F32Piece pc = q.piece(idx);
+    out[0] = pc.tile;
+    out[1] = pc.s_begin;
+    out[2] = pc.s_end;
+    out[3] = pc.from_partial ? 1 : 0;
+    out[4] = pc.to_partial ? 1 : 0;
+    return 1;
 }
 
 int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position)

@@ -100,6 +100,19 @@ __device__ __forceinline__ void tile_origin(int bm, int bn, int &m0, int &n0)
     n0 = (r / gm) * bn;
 }
 
+// The same walk for a linear tile index t of a persistent kernel (tiles_m x
+// tiles_n tiles): t takes the place of the CTA's linear block index.
+__device__ __forceinline__ void tile_origin_linear(int t, int tiles_m, int tiles_n, int bm, int bn, int &m0, int &n0)
+{
+    const int per_group = kGroupM * tiles_n;
+    const int group = t / per_group;
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, tiles_m - first_m);
+    const int r = t - group * per_group;
+    m0 = (first_m + r % gm) * bm;
+    n0 = (r / gm) * bn;
+}
+
 // One thread's micro-tile of C, held as pairs of adjacent columns: pair p of
 // row i is columns (2p, 2p+1) of the thread's TN columns, packed in one
 // 64-bit register pair so a single fma.rn.f32x2 updates both.
@@ -281,8 +294,9 @@ __device__ __forceinline__ float4 load_chunk_guarded(const float *__restrict__ b
 // valid address (the matrix base), never a skipped issue: a predicated-off
 // cp.async would leave stale data instead of zeros ("cp.async", section
 // "Predication is different from zero fill").
+template <int Form>
 __device__ __forceinline__ void cp_chunk_guarded(uint32_t dst, const float *__restrict__ base, long long ld, int r,
-                                                 int c, int R, int C, bool vec)
+                                                 int c, int R, int C, bool vec, uint64_t pol)
 {
     const bool row_ok = r < R;
     if (vec) {
@@ -292,13 +306,13 @@ __device__ __forceinline__ void cp_chunk_guarded(uint32_t dst, const float *__re
             nbytes = static_cast<uint32_t>(min(C - c, 4)) * 4u;
             src = base + static_cast<long long>(r) * ld + c;
         }
-        cp_async_cg16(dst, src, nbytes);
+        cp_async_cg16_f<Form>(dst, src, nbytes, pol);
     } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool ok = row_ok && (c + e) < C;
             const float *src = ok ? base + static_cast<long long>(r) * ld + c + e : base;
-            cp_async_ca4(dst + 4u * e, src, ok ? 4u : 0u);
+            cp_async_ca4_f<Form & 1>(dst + 4u * e, src, ok ? 4u : 0u);
         }
     }
 }
@@ -322,8 +336,11 @@ __device__ __forceinline__ void b_chunk_coords(int c, int k0, int n0, int &k, in
 // Issue this thread's cp.async copies of slice kt into the stage at `stage`
 // (A slice then B slice).  Completion is tracked by the caller: a commit
 // group (cp.async fill) or an mbarrier arrive (mbarrier-completed fill).
-template <class T>
-__device__ __forceinline__ void issue_slice_cpasync(float *stage, const F32Args &p, int tid, int m0, int n0, int kt)
+// `Form` selects the optional cache qualifiers (ptx.cuh, CopyForm) with the
+// L2 policies `pol_a`, `pol_b`; Form 0 is the plain copy.
+template <class T, int Form>
+__device__ __forceinline__ void issue_slice_cpasync_f(float *stage, const F32Args &p, int tid, int m0, int n0, int kt,
+                                                      uint64_t pol_a, uint64_t pol_b)
 {
     float *sA = stage;
     float *sB = stage + T::kAFloats;
@@ -336,14 +353,14 @@ __device__ __forceinline__ void issue_slice_cpasync(float *stage, const F32Args 
             const int c = tid + q * T::kThreads;
             int r, k;
             a_chunk_coords<T>(c, m0, k0, r, k);
-            cp_async_cg16_full(smem_u32(sA + 4 * c), p.A + static_cast<long long>(r) * p.lda + k);
+            cp_async_cg16_full_f<Form>(smem_u32(sA + 4 * c), p.A + static_cast<long long>(r) * p.lda + k, pol_a);
         }
 #pragma unroll
         for (int q = 0; q < T::kBChunksPerThread; ++q) {
             const int c = tid + q * T::kThreads;
             int k, n;
             b_chunk_coords<T>(c, k0, n0, k, n);
-            cp_async_cg16_full(smem_u32(sB + 4 * c), p.B + static_cast<long long>(k) * p.ldb + n);
+            cp_async_cg16_full_f<Form>(smem_u32(sB + 4 * c), p.B + static_cast<long long>(k) * p.ldb + n, pol_b);
         }
         return;
     }
@@ -352,16 +369,30 @@ __device__ __forceinline__ void issue_slice_cpasync(float *stage, const F32Args 
         const int c = tid + q * T::kThreads;
         int r, k;
         a_chunk_coords<T>(c, m0, k0, r, k);
-        cp_chunk_guarded(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec);
+        cp_chunk_guarded<Form>(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec, pol_a);
     }
 #pragma unroll
     for (int q = 0; q < T::kBChunksPerThread; ++q) {
         const int c = tid + q * T::kThreads;
         int k, n;
         b_chunk_coords<T>(c, k0, n0, k, n);
-        cp_chunk_guarded(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec);
+        cp_chunk_guarded<Form>(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec, pol_b);
     }
 }
+
+// The L2 policies a kernel of copy form CF hands to its copies: built once
+// per thread, and only by the forms that carry a cache hint.
+template <int CF>
+struct CopyPolicies {
+    uint64_t a = 0, b = 0;
+    __device__ __forceinline__ explicit CopyPolicies(const F32Args &p)
+    {
+        if constexpr ((CF & 2) != 0) {
+            a = l2_policy(p.pol_a);
+            b = l2_policy(p.pol_b);
+        }
+    }
+};
 
 // Write the micro-tile; rows >= M and columns >= N are skipped.
 template <class T>

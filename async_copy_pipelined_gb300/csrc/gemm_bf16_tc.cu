@@ -69,6 +69,7 @@
 //            chunk index XOR row mod 8, as the C tensor map's 128-byte
 //            swizzle expects.
 #include <cstring>
+#include <type_traits>
 
 #include "gemm_internal.h"
 #include "ptx.cuh"
@@ -263,6 +264,9 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&map_a);
             tma_prefetch_map(&map_b);
+            // Optional L2 policies (.L2::cache_hint) on the loads.
+            const bool hint = (p.copy_form & 2) != 0;
+            const uint64_t pol_a = hint ? l2_policy(p.pol_a) : 0, pol_b = hint ? l2_policy(p.pol_b) : 0;
             int f = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -279,11 +283,11 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                     const uint32_t dst = base + static_cast<uint32_t>(f % S) * T::kStageBytes;
                     const uint32_t full = ring.full_bar(f);
                     ring.producer_commit(f, T::kStageBytes);
-                    tma_load_2d(dst, &map_a, full, kb * BK, mb * BM);
+                    tma_load_2d_opt(dst, &map_a, full, kb * BK, mb * BM, hint, pol_a);
 #pragma unroll
                     for (int j = 0; j < BN / static_cast<int>(kBBoxCols); ++j)
-                        tma_load_2d(dst + T::kATileBytes + j * kBBoxBytes, &map_b, full,
-                                    nb * BN + j * static_cast<int>(kBBoxCols), kb * BK);
+                        tma_load_2d_opt(dst + T::kATileBytes + j * kBBoxBytes, &map_b, full,
+                                        nb * BN + j * static_cast<int>(kBBoxCols), kb * BK, hint, pol_b);
                 }
             }
             // Only the last S positions issued can still be in flight; each
@@ -343,34 +347,49 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                 // arrival, so whoever waits for it must give up.
                 const bool fill_it = f != p.withhold;
                 if constexpr (Fill == GEMM_FILL_CPASYNC) {
-                    if (tile_interior && (kb + 1) * BK <= p.K) {
-                        // Every chunk is a whole in-range 16-byte copy (the
-                        // planner requires 16-byte row pitches).
-                        if (fill_it) {
+                    // One stage of copies in cache-qualifier form F (CopyForm
+                    // in ptx.cuh; 0 is the plain copy).
+                    auto copy_stage = [&](auto form) {
+                        constexpr int F = decltype(form)::value;
+                        const uint64_t pol_a = F & 2 ? l2_policy(p.pol_a) : 0;
+                        const uint64_t pol_b = F & 2 ? l2_policy(p.pol_b) : 0;
+                        if (tile_interior && (kb + 1) * BK <= p.K) {
+                            // Every chunk is a whole in-range 16-byte copy (the
+                            // planner requires 16-byte row pitches); chunks
+                            // below BM * 8 belong to A.
+                            if (fill_it) {
+#pragma unroll
+                                for (int i = 0; i < kChunksPerThread; ++i)
+                                    cp_async_cg16_full_f<F>(dst + c_off[i], c_src[i],
+                                                            i * kCopyThreads < BM * 8 ? pol_a : pol_b);
+                            }
 #pragma unroll
                             for (int i = 0; i < kChunksPerThread; ++i)
-                                cp_async_cg16_full(dst + c_off[i], c_src[i]);
-                        }
-#pragma unroll
-                        for (int i = 0; i < kChunksPerThread; ++i)
-                            c_src[i] += c_step[i];
-                    } else if (fill_it) {
-                        for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
-                            int grow, gcol;
-                            bool is_a;
-                            uint32_t off;
-                            stage_chunk<MH>(q, mb, nb, kb, grow, gcol, is_a, off);
-                            const uint16_t *gbase = is_a ? p.A : p.B;
-                            const long long ld = is_a ? p.lda : p.ldb;
-                            const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
-                            uint32_t nbytes = 0;
-                            const uint16_t *src = gbase;
-                            if (grow < rows && gcol < cols) {
-                                nbytes = static_cast<uint32_t>(min(cols - gcol, 8)) * 2u;
-                                src = gbase + static_cast<long long>(grow) * ld + gcol;
+                                c_src[i] += c_step[i];
+                        } else if (fill_it) {
+                            for (int q = ptid; q < kStageChunks; q += kCopyThreads) {
+                                int grow, gcol;
+                                bool is_a;
+                                uint32_t off;
+                                stage_chunk<MH>(q, mb, nb, kb, grow, gcol, is_a, off);
+                                const uint16_t *gbase = is_a ? p.A : p.B;
+                                const long long ld = is_a ? p.lda : p.ldb;
+                                const int rows = is_a ? p.M : p.K, cols = is_a ? p.K : p.N;
+                                uint32_t nbytes = 0;
+                                const uint16_t *src = gbase;
+                                if (grow < rows && gcol < cols) {
+                                    nbytes = static_cast<uint32_t>(min(cols - gcol, 8)) * 2u;
+                                    src = gbase + static_cast<long long>(grow) * ld + gcol;
+                                }
+                                cp_async_cg16_f<F>(dst + off, src, nbytes, is_a ? pol_a : pol_b);
                             }
-                            cp_async_cg16(dst + off, src, nbytes);
                         }
+                    };
+                    switch (p.copy_form) {
+                    case 0: copy_stage(std::integral_constant<int, 0>{}); break;
+                    case 1: copy_stage(std::integral_constant<int, 1>{}); break;
+                    case 2: copy_stage(std::integral_constant<int, 2>{}); break;
+                    default: copy_stage(std::integral_constant<int, 3>{}); break;
                     }
                     cp_async_commit();
                     if (f >= kLag) {

@@ -21,7 +21,7 @@
 
 namespace pg {
 
-template <class T, int S>
+template <class T, int S, int CF>
 __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_kernel(const F32Args p)
 {
     static_assert(S >= 2 && S <= 6, "stages");
@@ -34,8 +34,9 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
     const int tc = tid % T::kThreadCols;
     const int k_slices = (p.K + T::BK - 1) / T::BK;
 
+    const CopyPolicies<CF> pol(p);
     auto issue = [&](int stage, int kt) {
-        issue_slice_cpasync<T>(smem + stage * T::kStageFloats, p, tid, m0, n0, kt);
+        issue_slice_cpasync_f<T, CF>(smem + stage * T::kStageFloats, p, tid, m0, n0, kt, pol.a, pol.b);
     };
 
     Accum<T> acc;
@@ -71,36 +72,50 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_k
     store_tile<T>(p, m0, n0, tr, tc, acc);
 }
 
-template <class T, int S>
+template <class T, int S, int CF>
 static int launch_cpasync_t(const F32Args &a, cudaStream_t s)
 {
     const int smem = S * T::kStageBytes;
     static std::atomic<unsigned long long> limit_set[kMaxDevices];
-    if (ensure_smem_limit(gemm_f32_cpasync_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
+    if (ensure_smem_limit(gemm_f32_cpasync_kernel<T, S, CF>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
-    gemm_f32_cpasync_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);
+    gemm_f32_cpasync_kernel<T, S, CF><<<grid, T::kThreads, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-template <class T>
+template <class T, int CF>
 static int launch_cpasync_tile(const F32Args &a, cudaStream_t s)
 {
     switch (a.stages) {
-    case 2: return launch_cpasync_t<T, 2>(a, s);
-    case 3: return launch_cpasync_t<T, 3>(a, s);
-    case 4: return launch_cpasync_t<T, 4>(a, s);
-    case 5: return launch_cpasync_t<T, 5>(a, s);
-    case 6: return launch_cpasync_t<T, 6>(a, s);
+    case 2: return launch_cpasync_t<T, 2, CF>(a, s);
+    case 3: return launch_cpasync_t<T, 3, CF>(a, s);
+    case 4: return launch_cpasync_t<T, 4, CF>(a, s);
+    case 5: return launch_cpasync_t<T, 5, CF>(a, s);
+    case 6: return launch_cpasync_t<T, 6, CF>(a, s);
     default: return GEMM_ERR_INVALID_ARG;
     }
 }
 
-int launch_f32_cpasync(const F32Args &a, cudaStream_t s)
+// The copy form (cache qualifiers) is a template parameter: the plain form's
+// kernels carry no trace of the optional ones (a run-time choice inside the
+// slice loop cost 2-3.5 % on GB300 at 4096^3).
+template <int CF>
+static int launch_cpasync_form(const F32Args &a, cudaStream_t s)
 {
     if (a.tile == 32)
-        return launch_cpasync_tile<TileXS>(a, s);
-    return a.tile == 128 ? launch_cpasync_tile<TileL>(a, s) : launch_cpasync_tile<TileS>(a, s);
+        return launch_cpasync_tile<TileXS, CF>(a, s);
+    return a.tile == 128 ? launch_cpasync_tile<TileL, CF>(a, s) : launch_cpasync_tile<TileS, CF>(a, s);
+}
+
+int launch_f32_cpasync(const F32Args &a, cudaStream_t s)
+{
+    switch (a.copy_form) {
+    case 0: return launch_cpasync_form<0>(a, s);
+    case 1: return launch_cpasync_form<1>(a, s);
+    case 2: return launch_cpasync_form<2>(a, s);
+    default: return launch_cpasync_form<3>(a, s);
+    }
 }
 
 } // namespace pg

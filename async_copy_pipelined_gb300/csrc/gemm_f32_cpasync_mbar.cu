@@ -28,7 +28,7 @@
 
 namespace pg {
 
-template <class T, int S>
+template <class T, int S, int CF>
 __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_mbar_kernel(const F32Args p)
 {
     static_assert(S >= 2 && S <= 6, "stages");
@@ -60,10 +60,11 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
     auto full_bar = [&](int f) { return full0 + 8u * static_cast<uint32_t>(f % S); };
     auto empty_bar = [&](int f) { return empty0 + 8u * static_cast<uint32_t>(f % S); };
     auto parity = [](int f) { return static_cast<uint32_t>((f / S) & 1); };
+    const CopyPolicies<CF> pol(p);
     auto issue = [&](int f) {
         if (f == p.withhold)
             return; // test hook: no copies and no arrival for this position
-        issue_slice_cpasync<T>(stage0 + (f % S) * T::kStageFloats, p, tid, m0, n0, f);
+        issue_slice_cpasync_f<T, CF>(stage0 + (f % S) * T::kStageFloats, p, tid, m0, n0, f, pol.a, pol.b);
         cp_async_mbar_arrive_noinc(full_bar(f));
     };
 
@@ -134,36 +135,48 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
         store_tile<T>(p, m0, n0, tr, tc, acc);
 }
 
-template <class T, int S>
+template <class T, int S, int CF>
 static int launch_cpasync_mbar_t(const F32Args &a, cudaStream_t s)
 {
     const int smem = f32_smem_bytes(T::BM, GEMM_FILL_CPASYNC_MBAR, S);
     static std::atomic<unsigned long long> limit_set[kMaxDevices];
-    if (ensure_smem_limit(gemm_f32_cpasync_mbar_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
+    if (ensure_smem_limit(gemm_f32_cpasync_mbar_kernel<T, S, CF>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
-    gemm_f32_cpasync_mbar_kernel<T, S><<<grid, T::kThreads, smem, s>>>(a);
+    gemm_f32_cpasync_mbar_kernel<T, S, CF><<<grid, T::kThreads, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-template <class T>
+template <class T, int CF>
 static int launch_cpasync_mbar_tile(const F32Args &a, cudaStream_t s)
 {
     switch (a.stages) {
-    case 2: return launch_cpasync_mbar_t<T, 2>(a, s);
-    case 3: return launch_cpasync_mbar_t<T, 3>(a, s);
-    case 4: return launch_cpasync_mbar_t<T, 4>(a, s);
-    case 5: return launch_cpasync_mbar_t<T, 5>(a, s);
-    case 6: return launch_cpasync_mbar_t<T, 6>(a, s);
+    case 2: return launch_cpasync_mbar_t<T, 2, CF>(a, s);
+    case 3: return launch_cpasync_mbar_t<T, 3, CF>(a, s);
+    case 4: return launch_cpasync_mbar_t<T, 4, CF>(a, s);
+    case 5: return launch_cpasync_mbar_t<T, 5, CF>(a, s);
+    case 6: return launch_cpasync_mbar_t<T, 6, CF>(a, s);
     default: return GEMM_ERR_INVALID_ARG;
     }
 }
 
-int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s)
+// The copy form is a template parameter, as for the group-completed fill.
+template <int CF>
+static int launch_cpasync_mbar_form(const F32Args &a, cudaStream_t s)
 {
     if (a.tile == 32)
-        return launch_cpasync_mbar_tile<TileXS>(a, s);
-    return a.tile == 128 ? launch_cpasync_mbar_tile<TileL>(a, s) : launch_cpasync_mbar_tile<TileS>(a, s);
+        return launch_cpasync_mbar_tile<TileXS, CF>(a, s);
+    return a.tile == 128 ? launch_cpasync_mbar_tile<TileL, CF>(a, s) : launch_cpasync_mbar_tile<TileS, CF>(a, s);
+}
+
+int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s)
+{
+    switch (a.copy_form) {
+    case 0: return launch_cpasync_mbar_form<0>(a, s);
+    case 1: return launch_cpasync_mbar_form<1>(a, s);
+    case 2: return launch_cpasync_mbar_form<2>(a, s);
+    default: return launch_cpasync_mbar_form<3>(a, s);
+    }
 }
 
 } // namespace pg

@@ -27,6 +27,16 @@ struct F32Args {
     unsigned int *status; // device status word
     unsigned long long wait_limit_ns;
     int withhold;          // ring position a producer leaves unfilled (test hook; -1: none)
+    int copy_form;         // cp.async qualifiers: bit 0 .L2::128B prefetch, bit 1 .L2::cache_hint
+    int pol_a, pol_b;      // L2 policy per operand: 0 normal, 1 evict_first, 2 evict_last
+    int tile_limit;        // one-tile TMA kernel: CTAs of linear tile index >= this exit at once
+    int ctas;              // split-region TMA kernel: CTAs launched (0: no split)
+    int split_ctas;        // what a split would use (planning; 0: nothing to split)
+    int split_region0;     // first tile of the split region (planning)
+    int withhold_handover; // test hook: hand-over flags are never raised
+    void *handover;        // persistent TMA kernel: accumulator hand-over space (nullptr: no split)
+    long long handover_bytes; // bytes a split of this call needs (0: the schedule has no split)
+    unsigned long long epoch; // value this call's ready flags carry
     int device;            // current device index
     unsigned long long ctx; // unique id of the current context (0: unknown)
 };
@@ -45,6 +55,8 @@ struct Bf16Args {
     unsigned int *status;
     unsigned long long wait_limit_ns;
     int withhold; // ring position the producers leave unfilled (test hook; -1: none)
+    int copy_form;     // as F32Args
+    int pol_a, pol_b;
     int num_sms;
     int device;
     unsigned long long ctx;
@@ -102,5 +114,6 @@ constexpr unsigned int kErrRoleProducer = 2u << 8;
 constexpr unsigned int kErrRoleMma = 3u << 8;
 constexpr unsigned int kErrRoleEpilogue = 4u << 8;
 constexpr unsigned int kErrRoleDrain = 5u << 8;
+constexpr unsigned int kErrRoleHandover = 6u << 8;
 
 } // namespace pg

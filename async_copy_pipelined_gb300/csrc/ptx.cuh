@@ -33,6 +33,77 @@ __device__ __forceinline__ void cp_async_cg16_full(uint32_t dst, const void *src
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Optional cache qualifiers of a cp.async copy ("cp.async" tile-op
+// reference, "Call parameters": a cache_policy operand; "Operand contract":
+// the .L2::64B / 128B / 256B prefetch size).  CopyForm bit 0: .L2::128B
+// prefetch; bit 1: .L2::cache_hint with a 64-bit policy from createpolicy.
+// Form 0 is the plain instruction.
+template <int Form>
+__device__ __forceinline__ void cp_async_cg16_full_f(uint32_t dst, const void *src, uint64_t pol)
+{
+    if constexpr (Form == 0)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+    else if constexpr (Form == 1)
+        asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+    else if constexpr (Form == 2)
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "l"(pol)
+                     : "memory");
+    else
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::128B [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                     "l"(pol)
+                     : "memory");
+}
+
+template <int Form>
+__device__ __forceinline__ void cp_async_cg16_f(uint32_t dst, const void *src, uint32_t src_bytes, uint64_t pol)
+{
+    if constexpr (Form == 0)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    else if constexpr (Form == 1)
+        asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                     "r"(src_bytes)
+                     : "memory");
+    else if constexpr (Form == 2)
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+                     "r"(src_bytes), "l"(pol)
+                     : "memory");
+    else
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::128B [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+                     "l"(src), "r"(src_bytes), "l"(pol)
+                     : "memory");
+}
+
+// The 4-byte .ca copy takes the prefetch qualifier only (Form bit 0): the
+// library never attaches a cache policy to it (see gemm_f32's option check).
+template <int Form>
+__device__ __forceinline__ void cp_async_ca4_f(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    static_assert(Form == 0 || Form == 1, "no cache policy on 4-byte copies");
+    if constexpr (Form == 0)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global.L2::128B [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+                     "r"(src_bytes)
+                     : "memory");
+}
+
+// L2 eviction policy for the .L2::cache_hint forms: kind 1 evict_first,
+// 2 evict_last, anything else evict_normal (the default behaviour), each for
+// the whole access (fraction 1.0).
+__device__ __forceinline__ uint64_t l2_policy(int kind)
+{
+    uint64_t p;
+    if (kind == 1)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    else if (kind == 2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+
 // 4-byte copy (.ca: the only cache qualifier allowed below 16 bytes).
 __device__ __forceinline__ void cp_async_ca4(uint32_t dst, const void *src, uint32_t src_bytes)
 {
@@ -135,6 +206,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// Flags between CTAs of one grid, in global memory: a release store after
+// this thread's (and, through a preceding CTA barrier, its CTA's) writes, and
+// an acquire load that orders the reads after it.
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long *addr, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *addr)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Wait until *flag == value, bounded like mbar_wait_bounded.
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned long long *flag, unsigned long long value,
+                                                  uint64_t limit_ns)
+{
+    if (ld_acquire_gpu_u64(flag) == value)
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t poll = 1; poll < kMaxPolls; ++poll) {
+        if (ld_acquire_gpu_u64(flag) == value)
+            return true;
+        if ((poll & 63u) == 0 && global_timer_ns() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
 // Record the first error of this launch sequence in the device status word.
 __device__ __forceinline__ void record_error(unsigned int *status, unsigned int code)
 {
@@ -158,6 +260,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// The same load carrying an L2 cache policy (.L2::cache_hint).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                 uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4}], [%2], %5;\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+// Either form: `hint` selects the cache-policy form (one elected thread
+// issues these, so a run-time choice costs nothing measurable).
+__device__ __forceinline__ void tma_load_2d_opt(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                bool hint, uint64_t pol)
+{
+    if (hint)
+        tma_load_2d_hint(dst, map, bar, x, y, pol);
+    else
+        tma_load_2d(dst, map, bar, x, y);
 }
 
 // 2-D tiled store of the box at coordinates (x = innermost, y) from shared

@@ -27,6 +27,11 @@ struct TmaRing {
     __device__ __forceinline__ uint32_t full_bar(int f) const { return full0 + 8u * static_cast<uint32_t>(f % S); }
     __device__ __forceinline__ uint32_t empty_bar(int f) const { return empty0 + 8u * static_cast<uint32_t>(f % S); }
     __device__ __forceinline__ static uint32_t parity(int f) { return static_cast<uint32_t>((f / S) & 1); }
+    // The same for unsigned positions: a position whose start is not known
+    // to the compiler (a persistent kernel's) then costs no sign fix-ups.
+    __device__ __forceinline__ uint32_t full_bar(unsigned f) const { return full0 + 8u * (f % S); }
+    __device__ __forceinline__ uint32_t empty_bar(unsigned f) const { return empty0 + 8u * (f % S); }
+    __device__ __forceinline__ static uint32_t parity(unsigned f) { return (f / S) & 1u; }
 
     // One thread, before the CTA barrier that publishes the ring.
     // full: `fills` arrivals per filling (1: the TMA producer's
@@ -42,25 +47,29 @@ struct TmaRing {
     }
 
     // Producer: wait until stage f % S has been released by its last user.
-    __device__ __forceinline__ bool producer_acquire(int f, uint64_t limit_ns) const
+    template <class F>
+    __device__ __forceinline__ bool producer_acquire(F f, uint64_t limit_ns) const
     {
         return mbar_wait_bounded(empty_bar(f), parity(f) ^ 1u, limit_ns);
     }
 
     // Producer: announce the bytes the copies of position f will deliver.
-    __device__ __forceinline__ void producer_commit(int f, uint32_t bytes) const
+    template <class F>
+    __device__ __forceinline__ void producer_commit(F f, uint32_t bytes) const
     {
         mbar_arrive_expect_tx(full_bar(f), bytes);
     }
 
     // Consumer: wait until every byte of position f has landed.
-    __device__ __forceinline__ bool consumer_wait(int f, uint64_t limit_ns) const
+    template <class F>
+    __device__ __forceinline__ bool consumer_wait(F f, uint64_t limit_ns) const
     {
         return mbar_wait_bounded(full_bar(f), parity(f), limit_ns);
     }
 
     // Consumer: one arrival on the stage's empty barrier.
-    __device__ __forceinline__ void consumer_release(int f) const { mbar_arrive(empty_bar(f)); }
+    template <class F>
+    __device__ __forceinline__ void consumer_release(F f) const { mbar_arrive(empty_bar(f)); }
 };
 
 // Round a shared-memory address up to `align` bytes (a power of two).

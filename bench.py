@@ -360,10 +360,46 @@ def to_device(x, cols, dev):
     return t.to(dev)[:, :cols]
 
 
-def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile):
+def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, options=(), workspace="auto"):
     if name.startswith("bf16"):
-        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile)
-    return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile)
+        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile, options=options)
+    return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile, options=options,
+                               workspace=workspace)
+
+
+# The cache qualifiers of the "cp.async" tile-op reference (prefetch size,
+# L2 cache policy), each timed beside the default call on the same operands.
+CACHE_OPTION_SETS = {"prefetch_128b": ("l2_prefetch_128b",),
+                     "a_first_b_last": ("a_evict_first", "b_evict_last"),
+                     "a_last_b_last": ("a_evict_last", "b_evict_last")}
+
+
+def time_cache_options(pg, name, Ad, Bd, Cd, legs, flush, launches, flops):
+    """{leg: {option set: TFLOP/s, ...}} for each (fill, stages, tile) leg;
+    option sets a fill does not take are skipped.  Bits are checked equal to
+    the default call's."""
+    import torch
+    out, n = {}, 0
+    for fill, stages, tile in legs:
+        row = {}
+        ref = None
+        for label, opts in [("default", ())] + list(CACHE_OPTION_SETS.items()):
+            if fill == "tma" and "l2_prefetch_128b" in opts:
+                continue
+            call = gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, opts)
+            call()
+            torch.cuda.synchronize()
+            check_status(pg, f"cache option {label}")
+            if ref is None:
+                ref = Cd.clone()
+            same = bool(torch.equal(Cd.view(torch.int32), ref.view(torch.int32)))
+            mean, best, med = time_kernel(pg, call, flush, launches)
+            n += launches + 1
+            row[label] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best, "bits_equal_default": same}
+        for v in row.values():
+            v["vs_default"] = v["tflops"] / row["default"]["tflops"]
+        out[f"{fill}/S{stages}/T{tile}"] = row
+    return out, n
 
 
 def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
@@ -624,6 +660,14 @@ def run_ours(args, dist: Dist):
                 fills[f"{f}/S{s}/T{t}"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
                                            "ms_median": med,
                                            "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
+            # The persistent TMA kernel without its split of the last round
+            # of tiles (no hand-over workspace): same bits, SMs idle through
+            # the partial last round.
+            c = gemm_call(pg, name, Ad, Bd, Cd, "tma", 4, 128, workspace=None)
+            mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
+            launches += args.sweep_launches
+            fills["tma/S4/T128/unsplit"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
+                                            "ms_median": med, "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
             t_sync = fills["sync/S1/T128"]["ms"]
             for v in fills.values():
                 v["t_sync_over_t"] = t_sync / v["ms"]
@@ -675,6 +719,11 @@ def run_ours(args, dist: Dist):
                 per_cfg[wname] = row
                 del Acd, Bcd, A4d, Ccd
             extras["fills_per_workload"] = per_cfg
+            # Cache qualifiers on the pipelined fills at 4096^3.
+            co, n = time_cache_options(pg, name, Ad, Bd, Cd, [("cpasync", 4, 128), ("cpasync_mbar", 4, 128),
+                                                               ("tma", 4, 128)], flush, args.sweep_launches, flops)
+            launches += n
+            extras["cache_options_f32_4096"] = co
             # BF16 tensor-core leg at its own full size.
             wb, Ab, Bb = load_workload("bf16_8192")
             Abd, Bbd = to_device(Ab, wb["K"], dev), to_device(Bb, wb["N"], dev)
@@ -721,6 +770,10 @@ def run_ours(args, dist: Dist):
             for v in bfills.values():
                 v["t_sync_over_t"] = bfills["sync/S1/T128"]["ms"] / v["ms"]
             extras["bf16_8192"]["fills"] = bfills
+            co, n = time_cache_options(pg, "bf16_8192", Abd, Bbd, Cbd, [("tma", 3, 256), ("cpasync", 3, 256)], flush,
+                                       args.sweep_launches, fb)
+            launches += n
+            extras["cache_options_bf16_8192"] = co
             del Abd, Bbd, Cbd
     sampler.stop()
     clocks = sampler.summary()

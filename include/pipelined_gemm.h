@@ -61,6 +61,7 @@
 #ifndef PIPELINED_GEMM_H
 #define PIPELINED_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -72,6 +73,33 @@ enum gemm_fill_mode {
     GEMM_FILL_CPASYNC = 1,
     GEMM_FILL_TMA = 2,
     GEMM_FILL_CPASYNC_MBAR = 3
+};
+
+/*
+ * Optional cache qualifiers, OR-ed into a call's fill_mode.  Off by default;
+ * none changes a result bit.  They are the two qualifiers the "cp.async"
+ * tile-op reference lists: the prefetch size of the operand contract
+ * (.L2::64B / 128B / 256B; 128 B is offered) and the cache_policy call
+ * parameter (an L2 eviction priority carried by .L2::cache_hint).
+ *
+ *   GEMM_OPT_L2_PREFETCH_128B   every 16-byte cp.async copy also prefetches
+ *                               its 128-byte L2 line (cp.async fills only).
+ *   GEMM_OPT_{A,B}_EVICT_FIRST  copies of A (or B) carry an evict_first /
+ *   GEMM_OPT_{A,B}_EVICT_LAST   evict_last L2 policy (cp.async and TMA fills).
+ *
+ * Asking for both priorities of one operand, an option a fill does not
+ * take (the register-path fill takes none), or an unknown bit returns
+ * GEMM_ERR_INVALID_ARG.  An L2 policy on a cp.async fill whose A or B rows
+ * are not 16-byte aligned (so copied 4 bytes at a time) returns
+ * GEMM_ERR_UNSUPPORTED: the 4-byte copies take the prefetch size only.
+ */
+enum gemm_fill_option {
+    GEMM_OPT_L2_PREFETCH_128B = 0x100,
+    GEMM_OPT_A_EVICT_FIRST = 0x200,
+    GEMM_OPT_A_EVICT_LAST = 0x400,
+    GEMM_OPT_B_EVICT_FIRST = 0x800,
+    GEMM_OPT_B_EVICT_LAST = 0x1000,
+    GEMM_OPT_MASK = 0x1F00
 };
 
 typedef enum gemm_status {
@@ -102,6 +130,11 @@ typedef struct gemm_plan {
     int grid_x;          /* CTAs launched along x                                      */
     int grid_y;          /* CTAs launched along y                                      */
     int k_slices;        /* ceil(K / block_k)                                          */
+    int options;         /* the GEMM_OPT_* bits the call carries                       */
+    int persistent_ctas; /* CTAs of the split-region kernel gemm_f32_ws would add (one
+                            per SM, each walking several tile pieces), or 0          */
+    int workspace_bytes; /* device workspace gemm_f32_ws can use to split the last round
+                            of tiles in K (0: this call has nothing to split)          */
 } gemm_plan;
 
 /*
@@ -115,7 +148,8 @@ typedef struct gemm_plan {
  *               M x N logical elements are written; columns N..ldc-1 are
  *               left untouched.
  *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA or
- *               GEMM_FILL_CPASYNC_MBAR.
+ *               GEMM_FILL_CPASYNC_MBAR, optionally OR-ed with GEMM_OPT_*
+ *               cache qualifiers.
  *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default of 4.
  *               Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
@@ -142,6 +176,43 @@ int gemm_f32(int M, int N, int K,
              float *C, int ldc,
              int fill_mode, int stages, int block_tile,
              void *stream);
+
+/*
+ * gemm_f32_ws: gemm_f32 with an optional device workspace.
+ *
+ * With the TMA fill's 128 x 128 tile, one CTA computes one tile, in rounds
+ * of one tile per SM.  When the tile count is not a multiple of the SM
+ * count, the last round would leave SMs idle.  Given `workspace`, the
+ * rounds but the last run as usual and the remaining
+ * SMs + (tiles mod SMs) tiles go to a second, persistent kernel of one CTA
+ * per SM (plan.persistent_ctas), launched right after on the same stream,
+ * which shares them out in equal runs of K slices.  A tile cut between two
+ * CTAs is computed in K order: the first computes its first slices and
+ * hands its float32 accumulators over through the workspace, the second
+ * continues from them.  Every element is still the same fused multiply-add
+ * chain over k ascending, so the result is bit for bit that of gemm_f32.
+ *
+ *   workspace        device memory of the current device, 16-byte aligned,
+ *                    at least plan.workspace_bytes long (gemm_f32_plan), or
+ *                    NULL to run without the split (exactly gemm_f32).  It
+ *                    needs no initialisation and holds nothing between calls,
+ *                    but one workspace serves one call at a time: calls that
+ *                    may overlap on the GPU (other streams) need their own.
+ *                    Ignored when plan.workspace_bytes is 0.
+ *   workspace_bytes  its size; smaller than needed: GEMM_ERR_INVALID_ARG.
+ *
+ * A CTA waits (bounded) for the CTA before it to hand a tile over; CTAs
+ * start in index order, so the one it waits for is running or done.  If
+ * the wait expires, GEMM_ERR_TIMEOUT is recorded (role 6) as for any wait.
+ * Other arguments, errors and ownership as gemm_f32.
+ */
+int gemm_f32_ws(int M, int N, int K,
+                const float *A, int lda,
+                const float *B, int ldb,
+                float *C, int ldc,
+                int fill_mode, int stages, int block_tile,
+                void *workspace, size_t workspace_bytes,
+                void *stream);
 
 /* gemm_f32_plan: validate exactly as gemm_f32 does and describe the launch it
  * would make, without touching the device.  `plan` is a host pointer. */
@@ -221,7 +292,8 @@ const char *gemm_status_string(int status);
  * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
  * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async),
  * bits 8-15 the waiting role (1 consumer, 2 producer, 3 MMA issuer,
- * 4 epilogue, 5 drain of copies or MMAs still in flight).
+ * 4 epilogue, 5 drain of copies or MMAs still in flight, 6 hand-over of
+ * accumulators between CTAs in gemm_f32_ws).
  *
  * The word is ONE per device (per CUDA context), shared by every call on
  * every stream and every host thread.  A kernel records only the first

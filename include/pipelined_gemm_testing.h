@@ -43,6 +43,27 @@ extern "C" {
  */
 int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position);
 
+/*
+ * gemm_testing_withhold_handover: with `on` non-zero, every later
+ * gemm_f32_ws call whose persistent kernel splits tiles between CTAs
+ * computes and stores the handed-over accumulators but never raises the
+ * ready flag, so each CTA waiting for one gives up after the wait limit and
+ * records GEMM_ERR_TIMEOUT with role 6.  0 restores normal operation.
+ * Returns GEMM_OK.
+ */
+int gemm_testing_withhold_handover(int on);
+
+/*
+ * gemm_testing_f32_piece: the work schedule of the persistent FP32 TMA
+ * kernel, computed on the host exactly as the kernel computes it: piece
+ * `idx` of CTA `cta` when `ctas` CTAs share `tiles` tiles of `k_slices` K
+ * slices, with the last round split (`split` non-zero) or not.  Returns 1
+ * and fills out[0..4] = {tile, first slice, end slice, starts from handed-over
+ * accumulators, hands its accumulators over}, or 0 when the CTA has no such
+ * piece (or an argument is out of range).  No device is touched.
+ */
+int gemm_testing_f32_piece(int tiles, int ctas, int k_slices, int split, int cta, int idx, int *out);
+
 #ifdef __cplusplus
 }
 #endif

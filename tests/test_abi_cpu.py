@@ -73,15 +73,28 @@ def _plan(M, N, K, lda=None, ldb=None, ldc=None, fill=2, stages=0, tile=0, a=256
 
 
 def test_plan_defaults_and_shapes(lib):
+    # The TMA fill's 128 tile: 1024 tiles = 6 rounds of 152 (the SM count
+    # when no device can be asked) + 112 leave a last round to split, done by
+    # one persistent CTA per SM whose hand-over space is one 64 KiB
+    # accumulator tile and an 8-byte flag per CTA.
     st, p = _plan(4096, 4096, 4096, fill=2)
     assert st == 0 and p["block_m"] == 128 and p["stages"] == 4 and p["threads"] == 288
     assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (32, 32, 256)
+    assert p["persistent_ctas"] == 152 and p["workspace_bytes"] == 152 * (65536 + 8)
+    assert p["smem_bytes"] == 4 * 16384 + 16 * 4 + 64 + 1024
+    st, p = _plan(152 * 128, 2 * 128, 256, fill=2)  # 304 tiles: whole rounds, nothing to split
+    assert st == 0 and p["persistent_ctas"] == 0 and p["workspace_bytes"] == 0
+    st, p = _plan(1024, 1024, 4096, fill=2, tile=128)  # 64 tiles: one round, fewer CTAs than SMs
+    assert st == 0 and p["persistent_ctas"] == 0 and p["workspace_bytes"] == 0
+    st, p = _plan(4096, 4096, 4096, fill=1)
+    assert st == 0 and p["persistent_ctas"] == 0 and p["workspace_bytes"] == 0
+    assert (p["grid_x"], p["grid_y"]) == (32, 32)
     st, p = _plan(1024, 1024, 1024, fill=1)
     assert st == 0 and p["block_m"] == 64 and p["threads"] == 256 and p["stages"] == 4
     assert (p["grid_x"], p["grid_y"]) == (16, 16)
     st, p = _plan(4096, 4096, 4096, fill=3, stages=4)
     assert st == 0 and p["threads"] == 256 and p["a_copy_bytes"] == 16
-    assert p["smem_bytes"] == 4 * 16384 + 16 * 4 + 1024
+    assert p["smem_bytes"] == 4 * 16384 + 16 * 4 + 64 + 1024
     st, p = _plan(256, 256, 256, fill=0)
     assert st == 0 and p["stages"] == 1 and p["smem_bytes"] == 8192
     st, p = _plan(3000, 5000, 1000, lda=1003, fill=1, tile=64)
@@ -215,3 +228,112 @@ def test_testing_hooks_validate_and_reset(lib):
     assert lib.gemm_testing_set_hooks(10_000_000, 3) == 0
     assert lib.gemm_testing_set_hooks(0, -1) == 0
     assert "gemm_testing_set_hooks" in _declared_functions()
+
+
+@pytest.mark.parametrize("fill,opts,ok", [
+    ("cpasync", ("l2_prefetch_128b",), True),
+    ("cpasync_mbar", ("l2_prefetch_128b", "a_evict_first", "b_evict_last"), True),
+    ("tma", ("a_evict_last", "b_evict_last"), True),
+    ("tma", ("l2_prefetch_128b",), False),       # a cp.async qualifier
+    ("sync", ("a_evict_first",), False),         # plain loads take no policy
+    ("cpasync", ("a_evict_first", "a_evict_last"), False),
+    ("tma", ("b_evict_first", "b_evict_last"), False),
+])
+def test_cache_options_accepted_where_they_apply(lib, fill, opts, ok):
+    """The cache-qualifier options of the "cp.async" tile-op reference
+    (prefetch size, L2 cache policy) are accepted only by fills whose copies
+    carry them, and the plan echoes them."""
+    if ok:
+        p = pg.plan_f32(256, 256, 256, fill=fill, stages=0 if fill == "sync" else 2, options=opts)
+        assert p["options"] == sum(pg.OPTIONS[o] for o in opts)
+    else:
+        with pytest.raises(pg.GemmError) as e:
+            pg.plan_f32(256, 256, 256, fill=fill, stages=0 if fill == "sync" else 2, options=opts)
+        assert e.value.status == 1
+
+
+def test_cache_options_bf16_and_unknown_bits(lib):
+    p = pg.plan_bf16(256, 256, 256, fill="cpasync", options=("l2_prefetch_128b", "b_evict_last"))
+    assert p["options"] == 0x100 | 0x1000
+    assert pg.plan_bf16(256, 256, 256, fill="tma", options=("a_evict_first",))["options"] == 0x200
+    for fill, opts in (("tma", ("l2_prefetch_128b",)), ("sync", ("b_evict_last",))):
+        with pytest.raises(pg.GemmError):
+            pg.plan_bf16(256, 256, 256, fill=fill, options=opts)
+    plan = pg.GemmPlan()
+    assert lib.gemm_f32_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2 | 0x2000, 2, 0, ctypes.byref(plan)) == 1
+    assert lib.gemm_f32_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2 | 0x80, 2, 0, ctypes.byref(plan)) == 1
+
+
+def _pieces(lib, tiles, ctas, k, split):
+    out = (ctypes.c_int * 5)()
+    per_cta = []
+    for c in range(ctas):
+        ps, idx = [], 0
+        while lib.gemm_testing_f32_piece(tiles, ctas, k, split, c, idx, out):
+            ps.append(tuple(out))
+            idx += 1
+        per_cta.append(ps)
+    return per_cta
+
+
+@pytest.mark.parametrize("tiles,ctas,k", [(1024, 152, 256), (960, 152, 63), (153, 152, 2), (208, 152, 5),
+                                          (305, 152, 7), (304, 152, 9), (100, 152, 16), (1, 1, 3),
+                                          (7, 3, 1), (7, 3, 2), (29, 4, 17), (5000, 148, 300)])
+@pytest.mark.parametrize("split", [0, 1])
+def test_persistent_schedule_covers_every_slice_once_in_k_order(lib, tiles, ctas, k, split):
+    """The persistent FP32 kernel's work schedule, computed by the library's
+    own code on the host: every (tile, K slice) is computed exactly once; a
+    tile computed in two pieces is cut at one slice, the first piece handing
+    its accumulators to the CTA right after, whose last piece it is; and
+    that CTA does at least as many slices before the hand-over as the
+    producing CTA does up to it, so a hand-over is normally ready in time."""
+    per_cta = _pieces(lib, tiles, ctas, k, split)
+    seen = {}
+    for c, ps in enumerate(per_cta):
+        for (t, s0, s1, frm, to) in ps:
+            assert 0 <= t < tiles and 0 <= s0 < s1 <= k
+            for sl in range(s0, s1):
+                assert (t, sl) not in seen, f"slice {sl} of tile {t} twice"
+                seen[(t, sl)] = c
+    assert len(seen) == tiles * k
+    heads = {}
+    for c, ps in enumerate(per_cta):
+        tos = [i for i, p in enumerate(ps) if p[4]]
+        frs = [i for i, p in enumerate(ps) if p[3]]
+        assert len(tos) <= 1 and len(frs) <= 1
+        if not split:
+            assert not tos and not frs
+        for i in tos:
+            t, s0, s1 = ps[i][:3]
+            assert s0 == 0 and s1 < k
+            heads[t] = (c, s1, sum(p[2] - p[1] for p in ps[:i + 1]))
+        for i in frs:
+            assert i == len(ps) - 1, "a continued tile is a CTA's last piece"
+    for c, ps in enumerate(per_cta):
+        for i, (t, s0, s1, frm, to) in enumerate(ps):
+            if frm:
+                hc, hend, h_done_at = heads[t]
+                assert hc == c - 1 and hend == s0 and s1 == k
+                # slices this CTA computes before starting the tail, against
+                # the slices the producing CTA computes up to its hand-over
+                before = sum(p[2] - p[1] for p in ps[:i])
+                assert before >= h_done_at, (before, h_done_at)
+    if split and tiles > ctas and tiles % ctas and k >= 2:
+        # balanced: every CTA's total slices within one of the mean
+        totals = [sum(p[2] - p[1] for p in ps) for ps in per_cta]
+        assert max(totals) - min(totals) <= 1
+
+
+def test_cache_policy_refused_on_four_byte_copies(lib):
+    """Rows that are not 16-byte aligned are copied 4 bytes at a time, and
+    those copies take the prefetch size but no L2 policy."""
+    p = pg.plan_f32(300, 260, 200, lda=203, fill="cpasync", stages=2, options=("l2_prefetch_128b",))
+    assert p["a_copy_bytes"] == 4 and p["options"] == 0x100
+    for fill in ("cpasync", "cpasync_mbar"):
+        with pytest.raises(pg.GemmError) as e:
+            pg.plan_f32(300, 260, 200, lda=203, fill=fill, stages=2, options=("a_evict_first",))
+        assert e.value.status == 3
+        with pytest.raises(pg.GemmError) as e:
+            pg.plan_f32(129, 513, 97, lda=100, fill=fill, stages=2, options=("b_evict_last",))
+        assert e.value.status == 3
+    assert pg.plan_f32(128, 512, 96, lda=100, fill="cpasync", stages=2, options=("b_evict_last",))["options"] == 0x1000

@@ -167,6 +167,26 @@ def test_workload_8192_sampled():
     assert pg.device_status()[0] == 0
 
 
+def test_workload_8192_normal_whole_output():
+    """The bf16 workload at full size (normal(0, 0.5) inputs, the bench's
+    launch configuration) over the whole output: every element within the
+    float32-accumulation bound of the exact-product oracle, and the relative
+    Frobenius error within the acceptance bound."""
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    w = inputs.WORKLOADS["bf16_8192"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.workload_operands("bf16_8192")
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    Bd = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).cuda()
+    got = pg.gemm_bf16(Ad, Bd)
+    assert pg.device_status()[0] == 0
+    got = got.cpu().numpy()
+    del Ad, Bd
+    want = oracle.gemm_bf16_f64(A, B, M, N, K)
+    _check(got, want, _abs_products(A, B, M, N, K), K, "8192^3 normal, whole output")
+
+
 def test_workload_8192_smallint_exact_whole_output():
     """Entries in {-2..2} at 8192^3: exact in bfloat16, and every partial sum
     is an integer of magnitude at most 4K < 2^24, so the FP32 accumulator is

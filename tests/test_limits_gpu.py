@@ -50,7 +50,14 @@ def test_f32_rows_at_the_grid_limit_with_64bit_offsets(fill, stages):
     M, N, K = 65535 * 128, 24, 132
     A = _smallint((M, K), 11, torch.float32)
     B = _smallint((K, N), 12, torch.float32)
-    assert pg.plan_f32(M, N, K, fill=fill, stages=stages, block_tile=128)["grid_y"] == 65535
+    plan = pg.plan_f32(M, N, K, fill=fill, stages=stages, block_tile=128)
+    if fill == "tma":
+        # persistent: one CTA per SM walks the 65535 tiles (the last round
+        # split between CTAs, 65535 not being a multiple of the SM count)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert plan["persistent_ctas"] == sms and plan["workspace_bytes"] > 0
+    else:
+        assert plan["grid_y"] == 65535
     C = pg.gemm_f32(A, B, fill=fill, stages=stages, block_tile=128)
     assert pg.device_status()[0] == 0
     rows = np.unique(np.concatenate([sample_rows(M, 16, seed=13, tiles=(128,)),
