@@ -72,6 +72,8 @@ def _bind(l):
     l.gemm_f32.restype = I
     l.gemm_f32_ws.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P]
     l.gemm_f32_ws.restype = I
+    l.gemm_f32_noalloc.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]
+    l.gemm_f32_noalloc.restype = I
     l.gemm_f32_plan.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, ctypes.POINTER(GemmPlan)]
     l.gemm_f32_plan.restype = I
     l.gemm_bf16.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P]

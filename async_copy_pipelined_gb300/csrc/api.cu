@@ -69,7 +69,7 @@ static std::atomic<int> g_hook_withhold_handover{0};
 // if the driver cannot say.  Per-context state (the status word's address,
 // raised shared-memory limits) is keyed on it, so a context created after
 // cudaDeviceReset starts afresh.
-static unsigned long long current_context_id()
+unsigned long long current_context_id()
 {
     using GetCurrentFn = CUresult (*)(CUcontext *);
     using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);

@@ -99,6 +99,9 @@ constexpr int kBf16BlockM = 128;
 constexpr int kBf16BlockN = 256;
 constexpr int kBf16BlockK = 64;
 
+// Unique id of the calling thread's current CUDA context (0 if unknown).
+unsigned long long current_context_id();
+
 // Encode a 2-D tiled tensor map (row-major rows x cols, pitch in bytes).
 // Returns GEMM_OK or GEMM_ERR_CUDA / GEMM_ERR_MISALIGNED.
 int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uint64_t cols, uint64_t rows,

@@ -214,6 +214,34 @@ int gemm_f32_ws(int M, int N, int K,
                 void *workspace, size_t workspace_bytes,
                 void *stream);
 
+/*
+ * gemm_f32_noalloc: gemm_f32_ws for callers that cannot allocate device
+ * memory -- an allocator that needs a GEMM while it is serving a request
+ * (cudaMalloc cannot be re-entered from there), code that runs on a fixed,
+ * pre-planned memory budget, or latency-bound code that must not call
+ * cudaMalloc / cudaFree, which may synchronise the whole device.  Not part of
+ * the pages' method: they have no counterpart.
+ *
+ * The split's hand-over space is a fixed array inside this library, sized
+ * for up to 160 SMs (10,487,040 bytes); every GPU that loads the library
+ * holds it until the process exits.  The call itself allocates and frees
+ * nothing.  Arguments, results and errors as gemm_f32, plus:
+ *   - GEMM_ERR_UNSUPPORTED when the current device has more SMs than the
+ *     array has room for (a call with nothing to split still runs);
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress), so make it before any stream capture;
+ *   - every call shares the one array.  It keeps the last call's contents,
+ *     and none of them needs clearing (each call's ready flags carry a value
+ *     no earlier call used), but calls that overlap on the GPU -- on other
+ *     streams, or from other host threads -- race on it: serialise them.
+ */
+int gemm_f32_noalloc(int M, int N, int K,
+                     const float *A, int lda,
+                     const float *B, int ldb,
+                     float *C, int ldc,
+                     int fill_mode, int stages, int block_tile,
+                     void *stream);
+
 /* gemm_f32_plan: validate exactly as gemm_f32 does and describe the launch it
  * would make, without touching the device.  `plan` is a host pointer. */
 int gemm_f32_plan(int M, int N, int K,
