@@ -27,7 +27,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libpipelined_gemm.so")
 
-FILL = {"sync": 0, "cpasync": 1, "tma": 2, "cpasync_mbar": 3}
+FILL = {"sync": 0, "cpasync": 1, "tma": 2, "cpasync_mbar": 3, "cpasync_ws": 4}
 # Cache-qualifier options (include/pipelined_gemm.h, GEMM_OPT_*), OR-ed into
 # the fill code: pass e.g. fill="cpasync", options=("l2_prefetch_128b",).
 OPTIONS = {"l2_prefetch_128b": 0x100, "a_evict_first": 0x200, "a_evict_last": 0x400, "b_evict_first": 0x800,

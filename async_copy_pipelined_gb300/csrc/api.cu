@@ -219,6 +219,8 @@ int encode_tensor_map_2d(void *map_out, int dtype_is_bf16, const void *base, uin
 // ------------------------------------------------------------ sizes
 int f32_threads(int tile, int fill)
 {
+    if (fill == GEMM_FILL_CPASYNC_WS)
+        return f32_cpasync_ws_threads(tile);
     return (tile == 32 ? 32 : 256) + (fill == GEMM_FILL_TMA ? 32 : 0);
 }
 
@@ -285,7 +287,8 @@ static int decode_options(int fill_mode, int *fill, int *copy_form, int *pol_a, 
         return GEMM_ERR_INVALID_ARG;
     if ((opts & GEMM_OPT_B_EVICT_FIRST) && (opts & GEMM_OPT_B_EVICT_LAST))
         return GEMM_ERR_INVALID_ARG;
-    const bool cpasync = *fill == GEMM_FILL_CPASYNC || *fill == GEMM_FILL_CPASYNC_MBAR;
+    const bool cpasync =
+        *fill == GEMM_FILL_CPASYNC || *fill == GEMM_FILL_CPASYNC_MBAR || *fill == GEMM_FILL_CPASYNC_WS;
     const bool policy = (opts & (GEMM_OPT_A_EVICT_FIRST | GEMM_OPT_A_EVICT_LAST | GEMM_OPT_B_EVICT_FIRST |
                                  GEMM_OPT_B_EVICT_LAST)) != 0;
     if ((opts & GEMM_OPT_L2_PREFETCH_128B) && !cpasync)
@@ -310,7 +313,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
         return GEMM_ERR_INVALID_ARG;
     if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA &&
-        fill != GEMM_FILL_CPASYNC_MBAR)
+        fill != GEMM_FILL_CPASYNC_MBAR && fill != GEMM_FILL_CPASYNC_WS)
         return GEMM_ERR_INVALID_ARG;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
         return GEMM_ERR_INVALID_ARG;
@@ -342,8 +345,9 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         return GEMM_ERR_MISALIGNED;
     // Rows that are not 16-byte aligned are copied 4 bytes at a time
     // (cp.async.ca); those copies carry no cache policy.
-    if ((copy_form & 2) != 0 && (fill == GEMM_FILL_CPASYNC || fill == GEMM_FILL_CPASYNC_MBAR) && K > 0 && work &&
-        (!a_vec || !b_vec))
+    if ((copy_form & 2) != 0 &&
+        (fill == GEMM_FILL_CPASYNC || fill == GEMM_FILL_CPASYNC_MBAR || fill == GEMM_FILL_CPASYNC_WS) && K > 0 &&
+        work && (!a_vec || !b_vec))
         return GEMM_ERR_UNSUPPORTED;
     const long long grid_y = (M + tile - 1) / tile;
     const long long grid_x = (N + tile - 1) / tile;
@@ -434,7 +438,7 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
     int fill, copy_form, pol_a, pol_b;
     if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
         return GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_CPASYNC_MBAR)
+    if (fill == GEMM_FILL_CPASYNC_MBAR || fill == GEMM_FILL_CPASYNC_WS)
         return GEMM_ERR_UNSUPPORTED;
     if (block_m != 0 && block_m != 128 && block_m != 256)
         return GEMM_ERR_INVALID_ARG;
@@ -612,6 +616,7 @@ int gemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, in
     case GEMM_FILL_SYNC: return launch_f32_sync(args, s);
     case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);
     case GEMM_FILL_CPASYNC_MBAR: return launch_f32_cpasync_mbar(args, s);
+    case GEMM_FILL_CPASYNC_WS: return launch_f32_cpasync_ws(args, s);
     default: return launch_f32_tma(args, s);
     }
 }

@@ -380,6 +380,73 @@ __device__ __forceinline__ void issue_slice_cpasync_f(float *stage, const F32Arg
     }
 }
 
+// A group of NP producer threads (thread ptid of them) copying their share
+// of a slice: the copies of issue_slice_cpasync_f, dealt over NP threads
+// instead of all of the tile's threads.  For an interior tile with 16-byte
+// rows, each thread's chunk addresses are worked out once per tile
+// (CpAsyncShare::init) and stepped per slice; other tiles and the K tail take
+// the guarded copies.
+template <class T, int NP>
+struct CpAsyncShare {
+    static constexpr int kA = T::kAFloats / 4 / NP; // A chunks per producer thread
+    static constexpr int kB = T::kBFloats / 4 / NP; // B chunks per producer thread
+    static_assert(kA * NP * 4 == T::kAFloats && kB * NP * 4 == T::kBFloats, "whole chunks per producer thread");
+    const float *src_a[kA];
+    const float *src_b[kB];
+    bool interior;
+
+    __device__ __forceinline__ void init(const F32Args &p, int ptid, int m0, int n0)
+    {
+        interior = p.a_vec && p.b_vec && m0 + T::BM <= p.M && n0 + T::BN <= p.N;
+#pragma unroll
+        for (int q = 0; q < kA; ++q) {
+            int r, k;
+            a_chunk_coords<T>(ptid + q * NP, m0, 0, r, k);
+            src_a[q] = p.A + static_cast<long long>(r) * p.lda + k;
+        }
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+            int k, n;
+            b_chunk_coords<T>(ptid + q * NP, 0, n0, k, n);
+            src_b[q] = p.B + static_cast<long long>(k) * p.ldb + n;
+        }
+    }
+
+    // Copies of slice kt into `stage`; the sources then step one slice on.
+    template <int Form>
+    __device__ __forceinline__ void issue(float *stage, const F32Args &p, int ptid, int m0, int n0, int kt,
+                                          uint64_t pol_a, uint64_t pol_b)
+    {
+        float *sA = stage;
+        float *sB = stage + T::kAFloats;
+        const int k0 = kt * T::BK;
+        if (interior && k0 + T::BK <= p.K) {
+#pragma unroll
+            for (int q = 0; q < kA; ++q)
+                cp_async_cg16_full_f<Form>(smem_u32(sA + 4 * (ptid + q * NP)), src_a[q] + k0, pol_a);
+#pragma unroll
+            for (int q = 0; q < kB; ++q)
+                cp_async_cg16_full_f<Form>(smem_u32(sB + 4 * (ptid + q * NP)),
+                                           src_b[q] + static_cast<long long>(k0) * p.ldb, pol_b);
+            return;
+        }
+#pragma unroll
+        for (int q = 0; q < kA; ++q) {
+            const int c = ptid + q * NP;
+            int r, k;
+            a_chunk_coords<T>(c, m0, k0, r, k);
+            cp_chunk_guarded<Form>(smem_u32(sA + 4 * c), p.A, p.lda, r, k, p.M, p.K, p.a_vec, pol_a);
+        }
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+            const int c = ptid + q * NP;
+            int k, n;
+            b_chunk_coords<T>(c, k0, n0, k, n);
+            cp_chunk_guarded<Form>(smem_u32(sB + 4 * c), p.B, p.ldb, k, n, p.K, p.N, p.b_vec, pol_b);
+        }
+    }
+};
+
 // The L2 policies a kernel of copy form CF hands to its copies: built once
 // per thread, and only by the forms that carry a cache hint.
 template <int CF>

@@ -85,6 +85,8 @@ int launch_f32_sync(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync(const F32Args &a, cudaStream_t s);
 int launch_f32_tma(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s);
+int launch_f32_cpasync_ws(const F32Args &a, cudaStream_t s);
+int f32_cpasync_ws_threads(int tile);
 int launch_f32_zero(const F32Args &a, cudaStream_t s);
 int launch_bf16(const Bf16Args &a, int fill, cudaStream_t s);
 int launch_bf16_zero(const Bf16Args &a, cudaStream_t s);
@@ -112,6 +114,7 @@ constexpr unsigned int kErrFamilyF32Tma = 1;
 constexpr unsigned int kErrFamilyBf16 = 2;
 constexpr unsigned int kErrFamilySelftest = 3;
 constexpr unsigned int kErrFamilyF32CpAsyncMbar = 4;
+constexpr unsigned int kErrFamilyF32CpAsyncWs = 5;
 constexpr unsigned int kErrRoleConsumer = 1u << 8;
 constexpr unsigned int kErrRoleProducer = 2u << 8;
 constexpr unsigned int kErrRoleMma = 3u << 8;

@@ -649,8 +649,8 @@ def run_ours(args, dist: Dist):
         if not is_bf16:
             fills = {}
             variants = [("sync", 1, 128), ("sync", 1, 64)]
-            variants += [(f, s, 128) for f in ("cpasync", "tma", "cpasync_mbar") for s in (2, 3, 4, 6)]
-            variants += [("cpasync", 2, 64), ("tma", 2, 64), ("cpasync_mbar", 2, 64)]
+            variants += [(f, s, 128) for f in ("cpasync", "tma", "cpasync_mbar", "cpasync_ws") for s in (2, 3, 4, 6)]
+            variants += [("cpasync", 2, 64), ("tma", 2, 64), ("cpasync_mbar", 2, 64), ("cpasync_ws", 2, 64)]
             if w["lda"] % 4:
                 variants = [v for v in variants if v[0] != "tma"]
             for f, s, t in variants:
@@ -680,7 +680,8 @@ def run_ours(args, dist: Dist):
             ft = 2.0 * wt["M"] * wt["N"] * wt["K"]
             tall = {}
             for f, s in (("sync", 1), ("cpasync", 2), ("cpasync", 4), ("cpasync", 6), ("tma", 2), ("tma", 4),
-                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4), ("cpasync_mbar", 6)):
+                         ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4), ("cpasync_mbar", 6),
+                         ("cpasync_ws", 2), ("cpasync_ws", 4), ("cpasync_ws", 6)):
                 c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
                 mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                 launches += args.sweep_launches
@@ -707,7 +708,8 @@ def run_ours(args, dist: Dist):
                 # the automatic choice.
                 for t in ((128, 64) if wname == "f32_ragged" else (0,)):
                     sfx = f"/T{t}" if t else ""
-                    for f, s in (("sync", 1), ("cpasync", 2), ("cpasync_mbar", 2), ("tma", 2), ("tma", 4)):
+                    for f, s in (("sync", 1), ("cpasync", 2), ("cpasync_mbar", 2), ("cpasync_ws", 4), ("tma", 2),
+                                 ("tma", 4)):
                         c = gemm_call(pg, wname, A4d if f == "tma" else Acd, Bcd, Ccd, f, s, t)
                         mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
                         launches += args.sweep_launches
@@ -721,7 +723,8 @@ def run_ours(args, dist: Dist):
             extras["fills_per_workload"] = per_cfg
             # Cache qualifiers on the pipelined fills at 4096^3.
             co, n = time_cache_options(pg, name, Ad, Bd, Cd, [("cpasync", 4, 128), ("cpasync_mbar", 4, 128),
-                                                               ("tma", 4, 128)], flush, args.sweep_launches, flops)
+                                                               ("cpasync_ws", 4, 128), ("tma", 4, 128)], flush,
+                                       args.sweep_launches, flops)
             launches += n
             extras["cache_options_f32_4096"] = co
             # BF16 tensor-core leg at its own full size.
@@ -874,7 +877,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="f32_4096",
                     choices=["f32_256", "f32_1024", "f32_4096", "f32_ragged", "f32_tallk", "bf16_8192"])
-    ap.add_argument("--fill", choices=["sync", "cpasync", "tma", "cpasync_mbar"], default=None)
+    ap.add_argument("--fill", choices=["sync", "cpasync", "tma", "cpasync_mbar", "cpasync_ws"], default=None)
     ap.add_argument("--stages", type=int, default=None)
     ap.add_argument("--tile", type=int, default=None)
     ap.add_argument("--sweep-launches", type=int, default=20)

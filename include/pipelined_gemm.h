@@ -26,6 +26,12 @@
  *                      to (day 74, "Results"; "A study on CUDA async
  *                      memcpy", "block-scoped pipeline").  Every thread
  *                      copies and computes; no CTA barrier in the loop.
+ *   GEMM_FILL_CPASYNC_WS
+ *                      the same cp.async copies and mbarrier completion,
+ *                      issued by one or two dedicated producer warps while
+ *                      the other warps only compute ("A study on CUDA async
+ *                      memcpy", "block-scoped pipeline": producers and
+ *                      consumers need not be the same threads).  FP32 only.
  *
  * Every FP32 fill runs the same per-thread FMA micro-kernel, so for every C
  * element the result is one float32 fused multiply-add chain over k
@@ -72,7 +78,8 @@ enum gemm_fill_mode {
     GEMM_FILL_SYNC = 0,
     GEMM_FILL_CPASYNC = 1,
     GEMM_FILL_TMA = 2,
-    GEMM_FILL_CPASYNC_MBAR = 3
+    GEMM_FILL_CPASYNC_MBAR = 3,
+    GEMM_FILL_CPASYNC_WS = 4
 };
 
 /*
@@ -147,9 +154,9 @@ typedef struct gemm_plan {
  *   C, ldc      device pointer, leading dimension >= max(N, 1).  Only the
  *               M x N logical elements are written; columns N..ldc-1 are
  *               left untouched.
- *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA or
- *               GEMM_FILL_CPASYNC_MBAR, optionally OR-ed with GEMM_OPT_*
- *               cache qualifiers.
+ *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA,
+ *               GEMM_FILL_CPASYNC_MBAR or GEMM_FILL_CPASYNC_WS, optionally
+ *               OR-ed with GEMM_OPT_* cache qualifiers.
  *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default of 4.
  *               Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
@@ -264,7 +271,8 @@ int gemm_f32_plan(int M, int N, int K,
  *               chunks with cp.async into the same swizzled stages), or
  *               GEMM_FILL_SYNC (the register path: sixteen producer warps
  *               load and store, one stage, loads and MMAs alternate).
- *               GEMM_FILL_CPASYNC_MBAR returns GEMM_ERR_UNSUPPORTED.
+ *               GEMM_FILL_CPASYNC_MBAR and GEMM_FILL_CPASYNC_WS return
+ *               GEMM_ERR_UNSUPPORTED.
  *   stages      TMA / cp.async: 2..4 with the 128-row tile (4 x 48 KiB
  *               stages fill shared memory), 2..3 with the 256-row tile
  *               (64 KiB stages), or 0 for the tile's default (4 or 3).
@@ -318,7 +326,8 @@ const char *gemm_status_string(int status);
  * on a wait and returned early; its C output is undefined), or
  * GEMM_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
- * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async),
+ * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async,
+ * 5 FP32 cp.async from producer warps),
  * bits 8-15 the waiting role (1 consumer, 2 producer, 3 MMA issuer,
  * 4 epilogue, 5 drain of copies or MMAs still in flight, 6 hand-over of
  * accumulators between CTAs in gemm_f32_ws).

@@ -28,8 +28,8 @@ extern "C" {
  *   withhold_position  ring position (0, 1, 2, ... counted per CTA over all
  *                      of its K slices, and over its tiles for the
  *                      persistent tensor-core kernel) that the producers of
- *                      the FP32 TMA fill, the FP32 mbarrier-completed
- *                      cp.async fill and all three BF16 fills leave
+ *                      the FP32 TMA fill, both FP32 mbarrier-completed
+ *                      cp.async fills and all three BF16 fills leave
  *                      unfilled: no copy is issued and no arrival (and, for
  *                      TMA, no expected-transaction count) is made for it.
  *                      -1 restores normal operation.  The FP32 sync and

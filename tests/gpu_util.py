@@ -10,7 +10,7 @@ from async_copy_pipelined_gb300 import inputs
 
 # (fill, stages, tile) combinations of the FP32 kernel family.
 F32_VARIANTS = [("sync", 1, 32), ("sync", 1, 64), ("sync", 1, 128)]
-F32_VARIANTS += [(f, s, t) for f in ("cpasync", "tma", "cpasync_mbar") for s in (2, 3, 4, 5, 6)
+F32_VARIANTS += [(f, s, t) for f in ("cpasync", "tma", "cpasync_mbar", "cpasync_ws") for s in (2, 3, 4, 5, 6)
                  for t in (32, 64, 128)]
 
 

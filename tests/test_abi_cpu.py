@@ -118,7 +118,7 @@ def test_plan_defaults_and_shapes(lib):
     (dict(M=4, N=4, K=4, lda=3), 1),
     (dict(M=4, N=4, K=4, ldb=3), 1),
     (dict(M=4, N=4, K=4, ldc=3), 1),
-    (dict(M=4, N=4, K=4, fill=4), 1),
+    (dict(M=4, N=4, K=4, fill=5), 1),
     (dict(M=4, N=4, K=4, fill=0, stages=2), 1),
     (dict(M=4, N=4, K=4, fill=1, stages=1), 1),
     (dict(M=4, N=4, K=4, fill=2, stages=7), 1),

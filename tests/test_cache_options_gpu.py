@@ -27,7 +27,8 @@ def _f32(A, B, M, N, K, fill, stages, tile, options=()):
 
 @pytest.mark.parametrize("opts", F32_OPTION_SETS)
 @pytest.mark.parametrize("fill,stages,tile", [("cpasync", 3, 128), ("cpasync", 2, 64), ("cpasync_mbar", 4, 128),
-                                              ("cpasync_mbar", 2, 32), ("tma", 4, 128), ("tma", 2, 64)])
+                                              ("cpasync_mbar", 2, 32), ("cpasync_ws", 4, 128), ("cpasync_ws", 2, 64),
+                                              ("tma", 4, 128), ("tma", 2, 64)])
 @pytest.mark.parametrize("M,N,K,lda", [(300, 260, 200, 203), (129, 513, 97, 100)])
 def test_f32_options_keep_bits(opts, fill, stages, tile, M, N, K, lda):
     if fill == "tma":

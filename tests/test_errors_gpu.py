@@ -43,7 +43,7 @@ def test_refusals_enqueue_nothing():
         (dict(fill="cpasync", stages=7), 1),
         (dict(fill="tma", stages=1), 1),
         (dict(fill="tma", block_tile=96), 1),
-        (dict(fill=5), 1),
+        (dict(fill=6), 1),
     ]
     for kw, code in cases:
         with pytest.raises(pg.GemmError) as e:

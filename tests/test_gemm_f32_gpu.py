@@ -101,7 +101,7 @@ def test_workload_1024_fills_bit_identical():
     outs = {}
     for fill, stages, tile in [("sync", 1, 64), ("cpasync", 2, 64), ("tma", 2, 64), ("sync", 1, 128),
                                ("cpasync", 4, 128), ("tma", 4, 128), ("cpasync_mbar", 2, 64),
-                               ("cpasync_mbar", 4, 128)]:
+                               ("cpasync_mbar", 4, 128), ("cpasync_ws", 2, 64), ("cpasync_ws", 4, 128)]:
         got, _ = run_f32(A, B, M, N, K, fill, stages, tile)
         outs[(fill, stages, tile)] = got
         assert_bitwise_equal(got, want32, f"1024^3 {fill}/S{stages}/T{tile}")
@@ -128,7 +128,7 @@ def test_workload_4096_stage_sweep_whole_output():
     ref = pg.gemm_f32(Ad, Bd, fill="sync", block_tile=128)
     for fill, stages in [("cpasync", 2), ("cpasync", 3), ("cpasync", 4), ("cpasync", 6),
                          ("tma", 2), ("tma", 3), ("tma", 4), ("tma", 6), ("cpasync_mbar", 2), ("cpasync_mbar", 4),
-                         ("cpasync_mbar", 6)]:
+                         ("cpasync_mbar", 6), ("cpasync_ws", 2), ("cpasync_ws", 4), ("cpasync_ws", 6)]:
         out = pg.gemm_f32(Ad, Bd, fill=fill, stages=stages, block_tile=128)
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"{fill}/S{stages} != sync"
     out64 = pg.gemm_f32(Ad, Bd, fill="tma", stages=4, block_tile=64)

@@ -24,7 +24,7 @@ import oracle
 pytestmark = pytest.mark.gpu
 
 TIMEOUT = 6
-FAMILY = {"f32_tma": 1, "bf16": 2, "f32_cpasync_mbar": 4}
+FAMILY = {"f32_tma": 1, "bf16": 2, "f32_cpasync_mbar": 4, "f32_cpasync_ws": 5}
 ROLE_DRAIN = 5
 LIMIT_NS = 10_000_000  # 10 ms
 
@@ -49,7 +49,9 @@ def _expect_timeout(pg, family: int, what: str):
 
 F32_CASES = [("tma", 2, 128), ("tma", 4, 128), ("tma", 6, 128), ("tma", 3, 64), ("tma", 2, 32), ("tma", 6, 32),
              ("cpasync_mbar", 2, 128), ("cpasync_mbar", 4, 128), ("cpasync_mbar", 3, 64),
-             ("cpasync_mbar", 2, 32), ("cpasync_mbar", 6, 32)]
+             ("cpasync_mbar", 2, 32), ("cpasync_mbar", 6, 32),
+             ("cpasync_ws", 2, 128), ("cpasync_ws", 4, 128), ("cpasync_ws", 3, 64), ("cpasync_ws", 2, 32),
+             ("cpasync_ws", 6, 32)]
 
 
 @pytest.mark.parametrize("withhold", [0, 1, 7])
