@@ -29,6 +29,9 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull; // 2 s
 // 1923 us at 4).  At one CTA per SM the fourth 32 KiB stage costs no
 // occupancy; the 64x64 tile's three CTAs per SM take 96 KiB.
 constexpr int kDefaultStagesF32 = 4;
+// The producer-warp cp.async fill runs best with two (GB300, 4096^3,
+// TFLOP/s for 2 / 3 / 4 / 6 stages: 57.8 / 56.4 / 55.4 / 56.6).
+constexpr int kDefaultStagesF32CpAsyncWs = 2;
 // BF16 ring depth: four 48 KiB stages for the 128-row tile, three 64 KiB
 // stages for the 256-row tile (four of those do not fit in 227 KiB).
 constexpr int kDefaultStagesBf16Tile128 = 4;
@@ -328,7 +331,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         stages = 1;
     } else {
         if (stages == 0)
-            stages = kDefaultStagesF32;
+            stages = fill == GEMM_FILL_CPASYNC_WS ? kDefaultStagesF32CpAsyncWs : kDefaultStagesF32;
         if (stages < 2 || stages > 6)
             return GEMM_ERR_INVALID_ARG;
     }

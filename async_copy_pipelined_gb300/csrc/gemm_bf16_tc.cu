@@ -53,7 +53,7 @@
 // output element, so all of them give the same bits.
 //
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ... in
-// groups of 2048 rows of tiles so the tiles in flight share A and B rows in
+// groups of 4096 rows of tiles so the tiles in flight share A and B rows in
 // L2.  Ragged M, N, K: TMA zero-fills out-of-range box elements (zeros add
 // nothing to the products), the TMA stores clip at the matrix edge, and the
 // plain-store epilogue (C not 16-byte aligned) guards each element.
@@ -87,7 +87,10 @@ constexpr uint32_t kBBoxCols = 64;                          // n per B box (128 
 constexpr uint32_t kBBoxBytes = kBBoxCols * BK * 2;         // 8 KiB
 constexpr uint32_t kBTileBytes = BN * BK * 2;               // 32 KiB
 constexpr uint32_t kTmemCols = 512;                         // two 128 x 256 FP32 accumulators
-constexpr int kGroupRows = 2048;                            // rows of tiles per raster group
+// Rows of tiles per raster group.  Measured on GB300 at 8192^3 (256-row
+// tile, ncu DRAM bytes per launch): 2048 rows 1112 MB, 4096 rows 1055 MB, at
+// equal time; L2 eviction policies on A and B moved neither by more than 5 %.
+constexpr int kGroupRows = 4096;
 constexpr int kEpiBoxCols = 32;                             // FP32 columns per staged store
 constexpr uint32_t kStagingBytes = 32 * kEpiBoxCols * 4;    // 4 KiB per epilogue warp
 

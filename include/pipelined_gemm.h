@@ -157,7 +157,8 @@ typedef struct gemm_plan {
  *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA,
  *               GEMM_FILL_CPASYNC_MBAR or GEMM_FILL_CPASYNC_WS, optionally
  *               OR-ed with GEMM_OPT_* cache qualifiers.
- *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default of 4.
+ *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default: 4, or 2
+ *               for GEMM_FILL_CPASYNC_WS.
  *               Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
  *               "Exercise").
