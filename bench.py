@@ -46,8 +46,7 @@ FP32_FMA_PER_SM_PER_CLK = 128        # FP32 lanes per SM on sm_100-family parts
 # follows from NVIDIA's H100 SXM5 datasheet: 989.4 dense BF16 TFLOP/s at the
 # 1830 MHz boost clock on 132 SMs = 4096 FLOP per SM per clock; NVIDIA's
 # Blackwell material states the fifth-generation tensor core doubles the
-# per-SM FP16/BF16 rate.  bench.py also measures it (tensor_rate_probe) when
-# the library provides the probe.
+# per-SM FP16/BF16 rate.
 BF16_DENSE_FLOP_PER_SM_PER_CLK = 8192
 FALLBACK_SM_MAX_MHZ = 2070.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -360,11 +359,47 @@ def to_device(x, cols, dev):
     return t.to(dev)[:, :cols]
 
 
+def f32_kernels_per_call(pg, M, N, K, lda, ldb, fill, stages, tile, workspace="auto") -> int:
+    """Kernel launches one device-buffer FP32 call makes: the TMA fill with a
+    hand-over workspace splits the last round of 128 x 128 tiles in K, which
+    takes the one-tile kernel for the whole rounds before it (if any) and the
+    persistent kernel for the split region; every other call is one launch."""
+    if fill != "tma" or workspace is None or M == 0 or N == 0:
+        return 1
+    p = pg.plan_f32(M, N, K, lda=lda, ldb=ldb, fill=fill, stages=stages, block_tile=tile)
+    ctas = p["persistent_ctas"]
+    if ctas <= 0:
+        return 1
+    return 2 if (p["grid_x"] * p["grid_y"]) // ctas >= 2 else 1
+
+
+class GemmCall:
+    """One library call on fixed operands; `kernels` is how many of the
+    library's kernels each call launches."""
+
+    def __init__(self, fn, kernels: int):
+        self.fn, self.kernels = fn, kernels
+
+    def __call__(self):
+        return self.fn()
+
+
 def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, options=(), workspace="auto"):
     if name.startswith("bf16"):
-        return lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile, options=options)
-    return lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile, options=options,
-                               workspace=workspace)
+        return GemmCall(lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile, options=options), 1)
+    k = f32_kernels_per_call(pg, Ad.shape[0], Bd.shape[1], Ad.shape[1], Ad.stride(0), Bd.stride(0), fill, stages,
+                             tile, workspace)
+    return GemmCall(lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile, options=options,
+                                        workspace=workspace), k)
+
+
+# Library kernel launches made by the measured calls of the side legs
+# (time_kernel, clocks_during, the cache-option bit checks).
+SIDE_LAUNCHES = {"n": 0}
+
+
+def _count(call, calls: int):
+    SIDE_LAUNCHES["n"] += calls * getattr(call, "kernels", 1)
 
 
 # The cache qualifiers of the "cp.async" tile-op reference (prefetch size,
@@ -388,6 +423,7 @@ def time_cache_options(pg, name, Ad, Bd, Cd, legs, flush, launches, flops):
                 continue
             call = gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, opts)
             call()
+            _count(call, 1)
             torch.cuda.synchronize()
             check_status(pg, f"cache option {label}")
             if ref is None:
@@ -416,6 +452,7 @@ def time_kernel(pg, call, flush, launches: int, warmup: int = 3):
         call()
         timer.end()
     torch.cuda.synchronize()
+    _count(call, launches)
     check_status(pg, "a timed side leg")
     d = timer.durations_ms()
     return statistics.mean(d), min(d), statistics.median(d)
@@ -436,8 +473,9 @@ def clocks_during(call, seconds: float, uuid):
         launches += 50
         torch.cuda.synchronize()
     sampler.stop()
+    _count(call, launches)
     out = sampler.summary()
-    out["launches"] = launches
+    out["calls"] = launches
     return out
 
 
@@ -638,7 +676,8 @@ def run_ours(args, dist: Dist):
         sampler.stop()
         print(json.dumps({"error": f"device status {st} ({detail:#x}) after the timed loop"}), flush=True)
         return 1
-    launches = args.steps
+    launches = args.steps * call.kernels
+    SIDE_LAUNCHES["n"] = 0
     ms_step = total_ms / args.steps
     value = dist.world * flops * args.steps / (total_ms / 1e3) / 1e12
     local_mean = statistics.mean(per)
@@ -656,7 +695,6 @@ def run_ours(args, dist: Dist):
             for f, s, t in variants:
                 c = gemm_call(pg, name, Ad, Bd, Cd, f, s, t)
                 mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
-                launches += args.sweep_launches
                 fills[f"{f}/S{s}/T{t}"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
                                            "ms_median": med,
                                            "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
@@ -665,7 +703,6 @@ def run_ours(args, dist: Dist):
             # the partial last round.
             c = gemm_call(pg, name, Ad, Bd, Cd, "tma", 4, 128, workspace=None)
             mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
-            launches += args.sweep_launches
             fills["tma/S4/T128/unsplit"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
                                             "ms_median": med, "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
             t_sync = fills["sync/S1/T128"]["ms"]
@@ -684,7 +721,6 @@ def run_ours(args, dist: Dist):
                          ("cpasync_ws", 2), ("cpasync_ws", 4), ("cpasync_ws", 6)):
                 c = gemm_call(pg, "f32_tallk", Atd, Btd, Ctd, f, s, 32)
                 mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
-                launches += args.sweep_launches
                 tall[f"{f}/S{s}/T32"] = {"us": mean * 1e3, "us_min": best * 1e3, "us_median": med * 1e3,
                                          "gflops": ft / (mean / 1e3) / 1e9}
             for v in tall.values():
@@ -712,7 +748,6 @@ def run_ours(args, dist: Dist):
                                  ("tma", 4)):
                         c = gemm_call(pg, wname, A4d if f == "tma" else Acd, Bcd, Ccd, f, s, t)
                         mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
-                        launches += args.sweep_launches
                         row[f"{f}/S{s}{sfx}"] = {"tflops": fc / (mean / 1e3) / 1e12, "us": mean * 1e3,
                                                  "us_min": best * 1e3, "us_median": med * 1e3}
                     for key, v in row.items():
@@ -725,7 +760,6 @@ def run_ours(args, dist: Dist):
             co, n = time_cache_options(pg, name, Ad, Bd, Cd, [("cpasync", 4, 128), ("cpasync_mbar", 4, 128),
                                                                ("cpasync_ws", 4, 128), ("tma", 4, 128)], flush,
                                        args.sweep_launches, flops)
-            launches += n
             extras["cache_options_f32_4096"] = co
             # BF16 tensor-core leg at its own full size.
             wb, Ab, Bb = load_workload("bf16_8192")
@@ -735,7 +769,6 @@ def run_ours(args, dist: Dist):
             pb = pg.plan_bf16(wb["M"], wb["N"], wb["K"], lda=wb["lda"])
             cb = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", pb["stages"], pb["block_m"])
             mean, best, med = time_kernel(pg, cb, flush, args.sweep_launches)
-            launches += args.sweep_launches
             tf = fb / (mean / 1e3) / 1e12
             roof_b = {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": UNIT, "frac": tf / bf16_peak,
                       "traffic": profiled_traffic(f"bf16_8192:tma/S{pb['stages']}/T{pb['block_m']}"),
@@ -749,7 +782,7 @@ def run_ours(args, dist: Dist):
             # this kernel runs back to back (the tensor cores draw enough power
             # to lower it).
             bclk = clocks_during(cb, 1.0, sampler.uuid)
-            launches += bclk.pop("launches", 0)
+            bclk.pop("calls", None)
             check_status(pg, "the BF16 clock sample")
             derived = {"per_sm_per_clk": BF16_DENSE_FLOP_PER_SM_PER_CLK, "sms": num_sms,
                        "at_max_clock": {"mhz": sm_max, "tflops": bf16_derived_peak_tflops(num_sms, sm_max)},
@@ -767,7 +800,6 @@ def run_ours(args, dist: Dist):
                             ("cpasync", 2, 256), ("cpasync", 3, 256), ("sync", 1, 256)):
                 c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, f, s, t)
                 m2, b2, md2 = time_kernel(pg, c, flush, args.sweep_launches)
-                launches += args.sweep_launches
                 bfills[f"{f}/S{s}/T{t}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2, "ms_min": b2,
                                             "ms_median": md2}
             for v in bfills.values():
@@ -775,7 +807,6 @@ def run_ours(args, dist: Dist):
             extras["bf16_8192"]["fills"] = bfills
             co, n = time_cache_options(pg, "bf16_8192", Abd, Bbd, Cbd, [("tma", 3, 256), ("cpasync", 3, 256)], flush,
                                        args.sweep_launches, fb)
-            launches += n
             extras["cache_options_bf16_8192"] = co
             del Abd, Bbd, Cbd
     sampler.stop()
@@ -807,8 +838,13 @@ def run_ours(args, dist: Dist):
         e2e = {"value": dist.world * flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": dist.world * int(Ah.element_size() * M * K + Bh.element_size() * K * N),
                "d2h_bytes_per_step": dist.world * int(4 * M * N), "ms_per_step": e_total / e_steps}
-        # One GEMM launch per row chunk of the host path, every step.
-        launches_e2e = e_steps * len(pg.host_row_chunks(M))
+        # The GEMM launches of the host path's row chunks, every step.
+        if is_bf16:
+            per_step = len(pg.host_row_chunks(M))
+        else:
+            per_step = sum(f32_kernels_per_call(pg, r1 - r0, N, K, K, N, leg["fill"], leg["stages"], leg["tile"])
+                           for r0, r1 in pg.host_row_chunks(M))
+        launches_e2e = e_steps * per_step
 
     kernel_key = f"{name}:{leg['fill']}/S{leg['stages']}/T{leg['tile']}"
     if is_bf16:
@@ -852,10 +888,10 @@ def run_ours(args, dist: Dist):
         "config": workload_config(name, w, {**leg, "gate": gate,
                                             "parallelism": "replicas" if dist.world > 1 else "single GPU"}),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": launches + (launches_e2e if e2e else 0),
-        "gpu_launches_breakdown": {"timed_steps": args.steps,
-                                                             "sweep_and_bf16_legs": launches - args.steps,
-                                                             "e2e_launches": launches_e2e if e2e else 0},
+        "gpu_launches": launches + SIDE_LAUNCHES["n"] + (launches_e2e if e2e else 0),
+        "gpu_launches_breakdown": {"timed_steps": launches, "kernels_per_step": call.kernels,
+                                   "sweep_and_bf16_legs": SIDE_LAUNCHES["n"],
+                                   "e2e_launches": launches_e2e if e2e else 0},
         "kernel_sources_sha": kernel_sources_sha(),
     }
     line.update(extras)
