@@ -32,8 +32,11 @@ FILL = {"sync": 0, "cpasync": 1, "tma": 2, "cpasync_mbar": 3, "cpasync_ws": 4}
 # the fill code: pass e.g. fill="cpasync", options=("l2_prefetch_128b",).
 OPTIONS = {"l2_prefetch_128b": 0x100, "a_evict_first": 0x200, "a_evict_last": 0x400, "b_evict_first": 0x800,
            "b_evict_last": 0x1000}
+# GEMM_OPT_ACCUMULATE: FP32 tiles start from C's values (gemm_f32(accumulate=True)).
+OPT_ACCUMULATE = 0x2000
 
 GEMM_OK = 0
+GEMM_ERR_TIMEOUT = 6
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_UNSUPPORTED",
                 4: "GEMM_ERR_ARCH", 5: "GEMM_ERR_CUDA", 6: "GEMM_ERR_TIMEOUT"}
 
@@ -94,6 +97,17 @@ def _bind(l):
     l.gemm_testing_withhold_handover.restype = I
     l.gemm_testing_f32_piece.argtypes = [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)]
     l.gemm_testing_f32_piece.restype = I
+    l.gemm_f32_host.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P, P]
+    l.gemm_f32_host.restype = I
+    l.gemm_f32_host_scratch.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_size_t)]
+    l.gemm_f32_host_scratch.restype = I
+    IP = ctypes.POINTER(ctypes.c_int)
+    l.gemm_f32_host_schedule.argtypes = [I, I, I, I, IP, I, IP, IP, I, IP]
+    l.gemm_f32_host_schedule.restype = I
+    l.gemm_testing_host_policy.argtypes = [I, I, I, I, I, I]
+    l.gemm_testing_host_policy.restype = I
+    l.gemm_testing_host_streams.argtypes = [I, I]
+    l.gemm_testing_host_streams.restype = I
     return l
 
 
@@ -206,26 +220,46 @@ def plan_bf16(M, N, K, lda=None, ldb=None, ldc=None, fill="tma", stages=0, block
     return p.as_dict()
 
 
-# Host-buffer calls move A and C in row chunks of at least this many rows,
-# issued round-robin on HOST_STREAMS streams that are created once per device.
-# Measured on GB300 at 4096^3 (FP32, host copies at about 190 GB/s each way):
-# eight 512-row chunks on four streams take 2.74 ms a call, four 1024-row
-# chunks on two streams 2.83 ms, and creating the streams on every call adds
-# about 0.1 ms more.
-HOST_CHUNK_MIN_ROWS = 512
-HOST_CHUNKS_MAX = 16
-HOST_STREAMS = 4
+# BF16 host-buffer calls (host tensors in, host C out) run on three streams
+# made once per device: one carries the host-to-device copies, one the GEMMs,
+# one the device-to-host copies, ordered by events, with C cut into row
+# chunks of about HOST_CHUNK_WAVES waves of 128 x 128 tiles so that each
+# chunk's copies overlap the GEMMs of others.  FP32 host-buffer calls go to
+# the library's native executor instead (gemm_f32_host in the C header).
+HOST_CHUNK_WAVES = 1.25
+HOST_CHUNK_MIN_ROWS = 256
+HOST_STREAMS = 3
 _host_streams = {}
+_host_sms = {}
+_host_scratch = {}
+_host_status = {}
 
 
-def host_row_chunks(M: int):
-    """Row ranges [r0, r1) the host-buffer path splits A and C into: up to
-    HOST_CHUNKS_MAX chunks of at least HOST_CHUNK_MIN_ROWS rows, each a whole
-    number of 128-row tiles except the last."""
-    n = max(1, min(HOST_CHUNKS_MAX, M // HOST_CHUNK_MIN_ROWS))
-    rows = -(-M // n)
-    rows = -(-rows // 128) * 128
+def host_chunk_rows(N: int, sms: int) -> int:
+    """Rows per chunk of the BF16 host path: enough 128 x 128 tiles for
+    HOST_CHUNK_WAVES waves on `sms` SMs, a multiple of 256 rows (whole tiles
+    of every kernel), at least HOST_CHUNK_MIN_ROWS."""
+    tiles_n = max(1, -(-N // 128))
+    tile_rows = -(-int(HOST_CHUNK_WAVES * sms) // tiles_n)
+    rows = max(HOST_CHUNK_MIN_ROWS, tile_rows * 128)
+    return -(-rows // 256) * 256
+
+
+def host_row_chunks(M: int, N: int, sms: int = 152):
+    """Row ranges [r0, r1) of the BF16 host path, in order."""
+    rows = host_chunk_rows(N, sms)
     return [(r0, min(M, r0 + rows)) for r0 in range(0, M, rows)]
+
+
+def host_schedule_f32(M: int, N: int, K: int, sms: int = 152):
+    """The cut the native FP32 host-buffer executor makes (no device is
+    touched): (K-block bounds, row-chunk bounds of the last block)."""
+    kb = (ctypes.c_int * 17)()
+    rb = (ctypes.c_int * 65)()
+    nk, nr = ctypes.c_int(), ctypes.c_int()
+    st = lib().gemm_f32_host_schedule(M, N, K, sms, kb, 17, ctypes.byref(nk), rb, 65, ctypes.byref(nr))
+    _check(st, "gemm_f32_host_schedule")
+    return list(kb[: nk.value + 1]), list(rb[: nr.value + 1])
 
 
 def _streams_for(dev):
@@ -236,41 +270,103 @@ def _streams_for(dev):
     return streams
 
 
-def _host_roundtrip(fn, A, B, C, dtype_out):
-    """Host tensors in, host C out.
+def _sms_of(dev) -> int:
+    import torch
+    n = _host_sms.get(dev.index)
+    if n is None:
+        n = _host_sms[dev.index] = torch.cuda.get_device_properties(dev).multi_processor_count
+    return n
 
-    B is copied to the device once.  A and C then move in row chunks on
-    HOST_STREAMS streams in turn, so the host-to-device copy of one chunk, the
-    GEMMs of others and the device-to-host copy of another overlap, and the
-    GEMM of the next chunk fills the SMs the last wave of the previous one
-    leaves idle.  Each C element is computed from the same row of A, the same
-    B and the same kernel arithmetic as in a single call, so chunking changes
-    no result bit.  Host tensors should be pinned for the copies to be
-    asynchronous.  Returns after C has been written."""
+
+def _f32_host_call(A, B, C, code, stages, block_tile):
+    """FP32 host tensors through the native executor (gemm_f32_host): the
+    device copies and the K-split hand-over space live in a scratch buffer
+    kept per device and grown as needed (the executor serialises its calls
+    on a device, so one buffer serves them all).  Returns once C is on the
+    host and the device status word has been checked."""
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
-    M, N = A.shape[0], B.shape[1]
+    M, K, lda, pa = _matrix_args(A, "A")
+    K2, N, ldb, pb = _matrix_args(B, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
+    if A.dtype != torch.float32 or B.dtype != torch.float32:
+        raise TypeError("gemm_f32 takes float32 tensors")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    Mc, Nc, ldc, pc = _matrix_args(C, "C")
+    if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
+        raise ValueError("C must be a float32 M x N tensor")
+    need = ctypes.c_size_t()
+    _check(lib().gemm_f32_host_scratch(M, N, K, ctypes.byref(need)), "gemm_f32_host_scratch")
+    scratch = _host_scratch.get(dev.index)
+    if scratch is None or scratch.numel() < need.value:
+        _host_scratch.pop(dev.index, None)
+        scratch = _host_scratch[dev.index] = torch.empty(max(need.value, 256), dtype=torch.uint8, device=dev)
+    word = _host_status.get(dev.index)
+    if word is None:
+        word = _host_status[dev.index] = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    cur = torch.cuda.current_stream(dev)
+    st = lib().gemm_f32_host(M, N, K, pa, lda, pb, ldb, pc, ldc, code, stages, block_tile, scratch.data_ptr(),
+                             scratch.numel(), word.data_ptr(), ctypes.c_void_p(cur.cuda_stream))
+    cur.synchronize()  # whatever was enqueued, even after an error, is done
+    _check(st, "gemm_f32_host")
+    # The executor copied the status word out after its last GEMM: a kernel
+    # that gave up on a bounded wait left its rows of C undefined.
+    detail = int(word[0]) & 0xFFFFFFFF
+    if detail:
+        _check(GEMM_ERR_TIMEOUT, f"host-buffer GEMM (device status word {detail:#x})")
+    return C
+
+
+def _host_roundtrip(fn, A, B, C, dtype_out):
+    """BF16 host tensors in, host C out.
+
+    fn(a, b, c, stream) runs the library's GEMM on device tensors, writing c.
+    Copies in, GEMMs and copies out each run in order on a stream of their
+    own: B first, then each row chunk's rows of A, its GEMM as soon as they
+    have landed, and its rows of C copied out as soon as the GEMM is done.
+    Each C element is computed from the same row of A, the same B and the
+    same arithmetic as in a single call, so the cutting changes no result
+    bit.  Host tensors should be pinned for the copies to be asynchronous.
+    The device buffers are allocated on the caller's current stream and held
+    until the call has synchronised, so no other work reuses them while the
+    side streams do.  Returns after C has been written."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M, K, N = A.shape[0], A.shape[1], B.shape[1]
     if C is None:
         C = torch.empty((M, N), dtype=dtype_out, pin_memory=True)
     cur = torch.cuda.current_stream(dev)
-    Bd = B.to(dev, non_blocking=True)
-    b_ready = torch.cuda.Event()
-    b_ready.record(cur)
-    streams = _streams_for(dev)
-    for i, (r0, r1) in enumerate(host_row_chunks(M)):
-        s = streams[i % len(streams)]
-        s.wait_event(b_ready)
-        with torch.cuda.stream(s):
-            # Allocated on stream s, so the caching allocator reuses these
-            # blocks only in s's order once they are released.
-            Ad = A[r0:r1].to(dev, non_blocking=True)
-            Cd = fn(Ad, Bd, s)
-            C[r0:r1].copy_(Cd, non_blocking=True)
-    for s in streams:
+    h2d, comp, d2h = _streams_for(dev)
+    Ad = torch.empty((M, K), dtype=A.dtype, device=dev)
+    Bd = torch.empty((K, N), dtype=B.dtype, device=dev)
+    Cd = torch.empty((M, N), dtype=dtype_out, device=dev)
+
+    def mark(stream):
+        e = torch.cuda.Event()
+        e.record(stream)
+        return e
+
+    start = mark(cur)  # the side streams begin after what `cur` already holds
+    for s in (h2d, comp, d2h):
+        s.wait_event(start)
+    with torch.cuda.stream(h2d):
+        Bd.copy_(B, non_blocking=True)
+    for r0, r1 in host_row_chunks(M, N, _sms_of(dev)):
+        with torch.cuda.stream(h2d):
+            Ad[r0:r1].copy_(A[r0:r1], non_blocking=True)
+        comp.wait_event(mark(h2d))  # this chunk's rows of A, and all of B before them
+        with torch.cuda.stream(comp):
+            fn(Ad[r0:r1], Bd, Cd[r0:r1], comp)
+        d2h.wait_event(mark(comp))
+        with torch.cuda.stream(d2h):
+            C[r0:r1].copy_(Cd[r0:r1], non_blocking=True)
+    for s in (h2d, comp, d2h):
         cur.wait_stream(s)
     cur.synchronize()
-    # Every chunk's GEMM is ordered before this point of `cur`: a kernel that
-    # gave up on a bounded wait left its rows of C undefined.
+    # Every GEMM is ordered before this point of `cur`: a kernel that gave up
+    # on a bounded wait left its rows of C undefined.
     st, detail = device_status(cur)
     _check(st, f"host-buffer GEMM (device status word {detail:#x})")
     return C
@@ -290,20 +386,29 @@ def _workspace(dev, stream_handle: int, nbytes: int):
     return buf
 
 
-def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, options=(), workspace="auto"):
+def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, options=(), workspace="auto",
+             accumulate=False):
     """C = A @ B in float32 through the library's FP32 kernel with the given fill.
 
     A (M x K), B (K x N) float32 tensors; C (M x N) float32 output, allocated
     if None.  CUDA tensors run on the device asynchronously on `stream`
-    (default: torch's current stream).  CPU tensors are copied to the current
-    device, computed and copied back, with the copies of row chunks
-    overlapping the GEMMs of others (see _host_roundtrip); the call returns
+    (default: torch's current stream).  CPU tensors go through the native
+    host-buffer executor (gemm_f32_host in the C header): B's rows and A's
+    columns cross the link in K blocks, each block's GEMM starts as soon as
+    it has landed and continues the FMA chains of the block before it, and
+    the last block's row chunks are copied out as they finish; the workspace
+    argument does not apply (the executor keeps its own).  The call returns
     once C is on the host, after the device status word has been checked
     (GemmError on a kernel timeout).
 
     options: cache-qualifier names from OPTIONS (GEMM_OPT_* in the C
     header): an L2 prefetch size for cp.async copies and L2 eviction
     priorities for A and B; none changes a result bit.
+
+    accumulate: C = C + A @ B, each element's FMA chain continuing from the
+    value C holds (GEMM_OPT_ACCUMULATE): a call over the first K0 columns
+    of A and rows of B followed by an accumulating call over the rest gives
+    the bits of one call over all K.  Needs C; device tensors only.
 
     workspace: hand-over space for the persistent TMA kernel's split of the
     last round of tiles (gemm_f32_ws in the C header).  "auto" keeps one
@@ -321,17 +426,10 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, o
     if not A.is_cuda:
         if C is not None:
             _refuse_aliased_output(C, A, B)
-        if block_tile == 0:
-            # The tile the whole problem would get, not what one row chunk
-            # alone would get.
-            try:
-                block_tile = plan_f32(A.shape[0], B.shape[1], A.shape[1], fill=fill, stages=stages)["block_m"]
-            except (RuntimeError, ValueError):
-                pass  # the chunk calls report the error
-        return _host_roundtrip(lambda a, b, s: gemm_f32(a, b, None, fill=fill, stages=stages,
-                                                        block_tile=block_tile, stream=s, options=options,
-                                                        workspace=workspace),
-                               A, B, C, torch.float32)
+        if accumulate:
+            raise ValueError("accumulate takes device tensors")
+        # block_tile 0: the executor picks the whole problem's tile.
+        return _f32_host_call(A, B, C, _fill_code(fill, options), stages, block_tile)
     if A.dtype != torch.float32 or B.dtype != torch.float32:
         raise TypeError("gemm_f32 takes float32 tensors")
     M, K, lda, pa = _matrix_args(A, "A")
@@ -339,12 +437,14 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, o
     if K2 != K:
         raise ValueError(f"inner dimensions differ: A is {M}x{K}, B is {K2}x{N}")
     if C is None:
+        if accumulate:
+            raise ValueError("accumulate needs C")
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
     Mc, Nc, ldc, pc = _matrix_args(C, "C")
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
     _refuse_aliased_output(C, A, B)
-    code = _fill_code(fill, options)
+    code = _fill_code(fill, options) | (OPT_ACCUMULATE if accumulate else 0)
     with torch.cuda.device(dev):
         sh = _stream_handle(stream)
         ws_ptr, ws_bytes = None, 0
@@ -384,8 +484,8 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, opt
                                     stages=stages)["block_m"]
             except (RuntimeError, ValueError):
                 pass  # the chunk calls report the error
-        return _host_roundtrip(lambda a, b, s: gemm_bf16(a, b, None, fill=fill, stages=stages, block_m=block_m,
-                                                         stream=s, options=options),
+        return _host_roundtrip(lambda a, b, c, s: gemm_bf16(a, b, c, fill=fill, stages=stages, block_m=block_m,
+                                                            stream=s, options=options),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")

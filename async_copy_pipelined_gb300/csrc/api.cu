@@ -29,6 +29,12 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull; // 2 s
 // 1923 us at 4).  At one CTA per SM the fourth 32 KiB stage costs no
 // occupancy; the 64x64 tile's three CTAs per SM take 96 KiB.
 constexpr int kDefaultStagesF32 = 4;
+// Except the TMA fill on the 128x128 tile, which runs best with two (GB300,
+// TFLOP/s for 2 / 3 / 4 / 6 stages: 61.3 / 60.3 / 61.0 / 60.4 at 4096^3,
+// 55.9 / - / 55.5 / - at 3000 x 5000 x 1000; with the K split of the last
+// round).  Its consumers chain slices, so two stages already keep a slice
+// in flight while one is computed.
+constexpr int kDefaultStagesF32TmaTile128 = 2;
 // The producer-warp cp.async fill runs best with two (GB300, 4096^3,
 // TFLOP/s for 2 / 3 / 4 / 6 stages: 57.8 / 56.4 / 55.4 / 56.6).
 constexpr int kDefaultStagesF32CpAsyncWs = 2;
@@ -259,6 +265,14 @@ int bf16_smem_bytes(int stages, int block_m)
 // ------------------------------------------------------------ planning
 // SMs of the current device for choosing a tile (cached once the device has
 // been checked), or kPlanningSms where there is no device to ask.
+static int planning_sms();
+
+int device_sms() { return planning_sms(); }
+
+int device_checked(int *dev) { return check_device(dev); }
+
+unsigned int *device_status_word(int dev, unsigned long long ctx) { return status_word(dev, ctx); }
+
 static int planning_sms()
 {
     int dev = 0;
@@ -274,16 +288,18 @@ static int planning_sms()
     return kPlanningSms;
 }
 
-// Split fill_mode into the fill (low byte) and the cache-qualifier options
-// (GEMM_OPT_*), and check that the options suit the fill: the prefetch size
-// is a cp.async qualifier; L2 policies go on cp.async and TMA copies, not on
-// the register path's plain loads.  Fills out the copy form and policies.
-static int decode_options(int fill_mode, int *fill, int *copy_form, int *pol_a, int *pol_b)
+// Split fill_mode into the fill (low byte) and the options (GEMM_OPT_*), and
+// check that the cache qualifiers suit the fill: the prefetch size is a
+// cp.async qualifier; L2 policies go on cp.async and TMA copies, not on the
+// register path's plain loads.  Fills out the copy form, the policies and
+// the accumulate flag.
+static int decode_options(int fill_mode, int *fill, int *copy_form, int *pol_a, int *pol_b, bool *accumulate)
 {
     const int opts = fill_mode & ~0xFF;
     *fill = fill_mode & 0xFF;
     *copy_form = 0;
     *pol_a = *pol_b = 0;
+    *accumulate = (opts & GEMM_OPT_ACCUMULATE) != 0;
     if (opts & ~GEMM_OPT_MASK)
         return GEMM_ERR_INVALID_ARG;
     if ((opts & GEMM_OPT_A_EVICT_FIRST) && (opts & GEMM_OPT_A_EVICT_LAST))
@@ -298,6 +314,9 @@ static int decode_options(int fill_mode, int *fill, int *copy_form, int *pol_a, 
         return GEMM_ERR_INVALID_ARG;
     if (policy && !cpasync && *fill != GEMM_FILL_TMA)
         return GEMM_ERR_INVALID_ARG;
+    // The kernels that start from C are built with plain copies only.
+    if (*accumulate && (opts & ~GEMM_OPT_ACCUMULATE) != 0)
+        return GEMM_ERR_UNSUPPORTED;
     *copy_form = ((opts & GEMM_OPT_L2_PREFETCH_128B) ? 1 : 0) | (policy ? 2 : 0);
     *pol_a = (opts & GEMM_OPT_A_EVICT_FIRST) ? 1 : (opts & GEMM_OPT_A_EVICT_LAST) ? 2 : 0;
     *pol_b = (opts & GEMM_OPT_B_EVICT_FIRST) ? 1 : (opts & GEMM_OPT_B_EVICT_LAST) ? 2 : 0;
@@ -313,8 +332,10 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
     int fill, copy_form, pol_a, pol_b;
-    if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
-        return GEMM_ERR_INVALID_ARG;
+    bool accumulate;
+    const int opt_status = decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b, &accumulate);
+    if (opt_status != GEMM_OK)
+        return opt_status;
     if (fill != GEMM_FILL_SYNC && fill != GEMM_FILL_CPASYNC && fill != GEMM_FILL_TMA &&
         fill != GEMM_FILL_CPASYNC_MBAR && fill != GEMM_FILL_CPASYNC_WS)
         return GEMM_ERR_INVALID_ARG;
@@ -329,11 +350,8 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         if (stages != 0 && stages != 1)
             return GEMM_ERR_INVALID_ARG;
         stages = 1;
-    } else {
-        if (stages == 0)
-            stages = fill == GEMM_FILL_CPASYNC_WS ? kDefaultStagesF32CpAsyncWs : kDefaultStagesF32;
-        if (stages < 2 || stages > 6)
-            return GEMM_ERR_INVALID_ARG;
+    } else if (stages != 0 && (stages < 2 || stages > 6)) {
+        return GEMM_ERR_INVALID_ARG;
     }
     if (tile == 0) {
         const long long t128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
@@ -341,6 +359,10 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     } else if (tile != 32 && tile != 64 && tile != 128) {
         return GEMM_ERR_INVALID_ARG;
     }
+    if (stages == 0)
+        stages = fill == GEMM_FILL_CPASYNC_WS               ? kDefaultStagesF32CpAsyncWs
+                 : (fill == GEMM_FILL_TMA && tile == 128) ? kDefaultStagesF32TmaTile128
+                                                          : kDefaultStagesF32;
     const bool a_vec = aligned16(A) && (lda % 4) == 0;
     const bool b_vec = aligned16(B) && (ldb % 4) == 0;
     const bool c_vec = aligned16(C) && (ldc % 4) == 0;
@@ -411,6 +433,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         args->a_vec = a_vec;
         args->b_vec = b_vec;
         args->c_vec = c_vec;
+        args->accumulate = accumulate;
         args->stages = stages;
         args->tile = tile;
         args->status = nullptr;
@@ -439,9 +462,11 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
     if (M < 0 || N < 0 || K < 0)
         return GEMM_ERR_INVALID_ARG;
     int fill, copy_form, pol_a, pol_b;
-    if (decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b) != GEMM_OK)
-        return GEMM_ERR_INVALID_ARG;
-    if (fill == GEMM_FILL_CPASYNC_MBAR || fill == GEMM_FILL_CPASYNC_WS)
+    bool accumulate;
+    const int opt_status = decode_options(fill_mode, &fill, &copy_form, &pol_a, &pol_b, &accumulate);
+    if (opt_status != GEMM_OK)
+        return opt_status;
+    if (fill == GEMM_FILL_CPASYNC_MBAR || fill == GEMM_FILL_CPASYNC_WS || accumulate)
         return GEMM_ERR_UNSUPPORTED;
     if (block_m != 0 && block_m != 128 && block_m != 256)
         return GEMM_ERR_INVALID_ARG;
@@ -613,8 +638,8 @@ int gemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, in
     if (!args.status)
         return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0)
-        return launch_f32_zero(args, s);
+    if (K == 0) // C = +0, or with accumulate C as it is
+        return args.accumulate ? GEMM_OK : launch_f32_zero(args, s);
     switch (fill_mode & 0xFF) {
     case GEMM_FILL_SYNC: return launch_f32_sync(args, s);
     case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);

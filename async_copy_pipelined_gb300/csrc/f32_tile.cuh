@@ -462,6 +462,46 @@ struct CopyPolicies {
 };
 
 // Write the micro-tile; rows >= M and columns >= N are skipped.
+// The accumulators a tile starts from: +0, or with ACC (GEMM_OPT_ACCUMULATE)
+// the values C holds, so that each element's FMA chain continues from C.
+// Loads follow store_tile's layout and guards; elements outside C stay +0
+// and are never stored.  ACC is a template parameter so that the kernels
+// without it compile exactly as before (a run-time flag here moved the K
+// loop's scheduling and cost 2 % at 4096^3).
+template <class T, bool ACC>
+__device__ __forceinline__ void init_tile(const F32Args &p, int m0, int n0, int tr, int tc, Accum<T> &acc)
+{
+    acc.zero();
+    if constexpr (!ACC)
+        return;
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i) {
+        const int row = m0 + tr + i * T::kThreadRows;
+        if (row >= p.M)
+            continue;
+        const float *crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll
+        for (int g = 0; g < T::kColGroups; ++g) {
+            const int col = n0 + g * T::kColGroupStride + tc * 4;
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (p.c_vec && col + 4 <= p.N) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(crow + col);
+                v[0] = c4.x;
+                v[1] = c4.y;
+                v[2] = c4.z;
+                v[3] = c4.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < p.N)
+                        v[e] = crow[col + e];
+            }
+            acc.pair[i][2 * g] = pack_f32x2(v[0], v[1]);
+            acc.pair[i][2 * g + 1] = pack_f32x2(v[2], v[3]);
+        }
+    }
+}
+
 template <class T>
 __device__ __forceinline__ void store_tile(const F32Args &p, int m0, int n0, int tr, int tc, const Accum<T> &acc)
 {

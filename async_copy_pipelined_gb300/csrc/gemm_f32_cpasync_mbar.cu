@@ -28,9 +28,13 @@
 
 namespace pg {
 
-template <class T, int S, int CF>
+template <class T, int S, int OPT>
 __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_mbar_kernel(const F32Args p)
 {
+    // OPT: the copy form (cache qualifiers, 0..3), or 4 for plain copies
+    // with the accumulators starting from C (GEMM_OPT_ACCUMULATE).
+    constexpr int CF = OPT & 3;
+    constexpr bool ACC = (OPT & 4) != 0;
     static_assert(S >= 2 && S <= 6, "stages");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = align_smem(smem_u32(smem_raw), 1024);
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_cpasync_m
     };
 
     Accum<T> acc;
-    acc.zero();
+    init_tile<T, ACC>(p, m0, n0, tr, tc, acc);
     bool ok = true;
 
     // Lookahead: S-1 slices issued at the top of each slice for two stages;
@@ -171,6 +175,8 @@ static int launch_cpasync_mbar_form(const F32Args &a, cudaStream_t s)
 
 int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s)
 {
+    if (a.accumulate) // plain copies only: the planner refuses accumulate with cache qualifiers
+        return launch_cpasync_mbar_form<4>(a, s);
     switch (a.copy_form) {
     case 0: return launch_cpasync_mbar_form<0>(a, s);
     case 1: return launch_cpasync_mbar_form<1>(a, s);

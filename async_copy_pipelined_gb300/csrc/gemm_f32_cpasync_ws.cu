@@ -28,9 +28,13 @@ constexpr int ws_producer_threads() { return T::kThreads >= 256 && T::BM == 128 
 template <class T>
 constexpr int ws_threads() { return T::kThreads + ws_producer_threads<T>(); }
 
-template <class T, int S, int CF>
+template <class T, int S, int OPT>
 __global__ void __launch_bounds__(ws_threads<T>(), T::kMinBlocksTma) gemm_f32_cpasync_ws_kernel(const F32Args p)
 {
+    // OPT: the copy form (cache qualifiers, 0..3), or 4 for plain copies
+    // with the accumulators starting from C (GEMM_OPT_ACCUMULATE).
+    constexpr int CF = OPT & 3;
+    constexpr bool ACC = (OPT & 4) != 0;
     static_assert(S >= 2 && S <= 6, "stages");
     constexpr int NP = ws_producer_threads<T>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(ws_threads<T>(), T::kMinBlocksTma) gemm_f32_cp
     const int tr = tid / T::kThreadCols;
     const int tc = tid % T::kThreadCols;
     Accum<T> acc;
-    acc.zero();
+    init_tile<T, ACC>(p, m0, n0, tr, tc, acc);
 
     auto stage_of = [&](int kt) { return stage0 + (kt % S) * T::kStageFloats; };
     auto wait_full = [&](int kt) {
@@ -152,6 +156,8 @@ static int launch_cpasync_ws_form(const F32Args &a, cudaStream_t s)
 
 int launch_f32_cpasync_ws(const F32Args &a, cudaStream_t s)
 {
+    if (a.accumulate) // plain copies only: the planner refuses accumulate with cache qualifiers
+        return launch_cpasync_ws_form<4>(a, s);
     switch (a.copy_form) {
     case 0: return launch_cpasync_ws_form<0>(a, s);
     case 1: return launch_cpasync_ws_form<1>(a, s);

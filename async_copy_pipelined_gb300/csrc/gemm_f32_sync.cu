@@ -12,7 +12,7 @@
 
 namespace pg {
 
-template <class T>
+template <class T, bool ACC>
 __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_sync_kernel(const F32Args p)
 {
     extern __shared__ __align__(1024) float smem[];
@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(T::kThreads, T::kMinBlocks) gemm_f32_sync_kern
     const int tc = tid % T::kThreadCols;
 
     Accum<T> acc;
-    acc.zero();
+    init_tile<T, ACC>(p, m0, n0, tr, tc, acc);
 
     const int k_slices = (p.K + T::BK - 1) / T::BK;
     for (int kt = 0; kt < k_slices; ++kt) {
@@ -72,16 +72,22 @@ __global__ void gemm_f32_zero_kernel(const F32Args p)
     }
 }
 
-template <class T>
-static int launch_sync_t(const F32Args &a, cudaStream_t s)
+template <class T, bool ACC>
+static int launch_sync_acc(const F32Args &a, cudaStream_t s)
 {
     const int smem = T::kStageBytes;
     static std::atomic<unsigned long long> limit_set[kMaxDevices];
-    if (ensure_smem_limit(gemm_f32_sync_kernel<T>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
+    if (ensure_smem_limit(gemm_f32_sync_kernel<T, ACC>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
-    gemm_f32_sync_kernel<T><<<grid, T::kThreads, smem, s>>>(a);
+    gemm_f32_sync_kernel<T, ACC><<<grid, T::kThreads, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+template <class T>
+static int launch_sync_t(const F32Args &a, cudaStream_t s)
+{
+    return a.accumulate ? launch_sync_acc<T, true>(a, s) : launch_sync_acc<T, false>(a, s);
 }
 
 int launch_f32_sync(const F32Args &a, cudaStream_t s)

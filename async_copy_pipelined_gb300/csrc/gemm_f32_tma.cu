@@ -29,7 +29,7 @@ namespace pg {
 template <class T>
 constexpr int tma_threads() { return T::kThreads + 32; }
 
-template <class T, int S>
+template <class T, int S, bool ACC>
 __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
     gemm_f32_tma_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const F32Args p)
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
     const int tr = tid / T::kThreadCols;
     const int tc = tid % T::kThreadCols;
     Accum<T> acc;
-    acc.zero();
+    init_tile<T, ACC>(p, m0, n0, tr, tc, acc);
 
     auto stage_of = [&](int kt) { return stage0 + (kt % S) * T::kStageFloats; };
     auto wait_full = [&](int kt) {
@@ -200,7 +200,7 @@ __device__ __noinline__ void f32_handover_publish(unsigned long long *flag, unsi
     }
 }
 
-template <int S>
+template <int S, bool ACC>
 __global__ void __launch_bounds__(TileL::kThreads + 32, 1)
     gemm_f32_tma_persistent_kernel(const __grid_constant__ CUtensorMap map_a,
                                    const __grid_constant__ CUtensorMap map_b, const F32Args p)
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(TileL::kThreads + 32, 1)
                 acc.pair[j / 2][2 * (j % 2) + 1] = v.y;
             }
         } else {
-            acc.zero();
+            init_tile<T, ACC>(p, m0, n0, tr, tc, acc);
         }
         const unsigned f_end = f0 + static_cast<unsigned>(pc.s_end - pc.s_begin);
         FragPipe<T> frag;
@@ -365,20 +365,20 @@ __global__ void __launch_bounds__(TileL::kThreads + 32, 1)
     }
 }
 
-template <int S>
+template <int S, bool ACC>
 static int launch_tma_persistent_t(const F32Args &a, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                    cudaStream_t s)
 {
     const int smem = f32_smem_bytes(128, GEMM_FILL_TMA, S);
     static std::atomic<unsigned long long> limit_set[kMaxDevices];
-    if (ensure_smem_limit(gemm_f32_tma_persistent_kernel<S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
+    if (ensure_smem_limit(gemm_f32_tma_persistent_kernel<S, ACC>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
-    gemm_f32_tma_persistent_kernel<S><<<a.ctas, tma_threads<TileL>(), smem, s>>>(map_a, map_b, a);
+    gemm_f32_tma_persistent_kernel<S, ACC><<<a.ctas, tma_threads<TileL>(), smem, s>>>(map_a, map_b, a);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-template <class T, int S>
-static int launch_tma_t(const F32Args &a, cudaStream_t s)
+template <class T, int S, bool ACC>
+static int launch_tma_acc(const F32Args &a, cudaStream_t s)
 {
     alignas(64) CUtensorMap map_a;
     alignas(64) CUtensorMap map_b;
@@ -393,19 +393,25 @@ static int launch_tma_t(const F32Args &a, cudaStream_t s)
         return st;
     const int smem = f32_smem_bytes(T::BM, GEMM_FILL_TMA, S);
     static std::atomic<unsigned long long> limit_set[kMaxDevices];
-    if (ensure_smem_limit(gemm_f32_tma_kernel<T, S>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
+    if (ensure_smem_limit(gemm_f32_tma_kernel<T, S, ACC>, smem, a.device, a.ctx, limit_set) != GEMM_OK)
         return GEMM_ERR_CUDA;
     const dim3 grid((a.N + T::BN - 1) / T::BN, (a.M + T::BM - 1) / T::BM);
     if (a.tile_limit > 0) {
-        gemm_f32_tma_kernel<T, S><<<grid, tma_threads<T>(), smem, s>>>(map_a, map_b, a);
+        gemm_f32_tma_kernel<T, S, ACC><<<grid, tma_threads<T>(), smem, s>>>(map_a, map_b, a);
         if (cudaGetLastError() != cudaSuccess)
             return GEMM_ERR_CUDA;
     }
     if constexpr (T::BM == 128) {
         if (a.ctas > 0) // the split region, after the whole rounds on the same stream
-            return launch_tma_persistent_t<S>(a, map_a, map_b, s);
+            return launch_tma_persistent_t<S, ACC>(a, map_a, map_b, s);
     }
     return GEMM_OK;
+}
+
+template <class T, int S>
+static int launch_tma_t(const F32Args &a, cudaStream_t s)
+{
+    return a.accumulate ? launch_tma_acc<T, S, true>(a, s) : launch_tma_acc<T, S, false>(a, s);
 }
 
 template <class T>

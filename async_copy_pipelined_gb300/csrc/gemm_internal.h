@@ -22,6 +22,7 @@ struct F32Args {
     bool a_vec; // A base and row pitch allow 16-byte copies
     bool b_vec; // same for B
     bool c_vec; // C base and ldc allow float4 stores
+    bool accumulate; // tiles start from C's values instead of +0
     int stages;
     int tile; // 64 or 128
     unsigned int *status; // device status word
@@ -103,6 +104,15 @@ constexpr int kBf16BlockK = 64;
 
 // Unique id of the calling thread's current CUDA context (0 if unknown).
 unsigned long long current_context_id();
+
+// SM count of the current device (152 where no device can be asked).
+int device_sms();
+
+// The current device, checked to be an sm_103 part: GEMM_OK or an error.
+int device_checked(int *dev);
+
+// Device address of the library's status word in context `ctx` of `dev`.
+unsigned int *device_status_word(int dev, unsigned long long ctx);
 
 // Encode a 2-D tiled tensor map (row-major rows x cols, pitch in bytes).
 // Returns GEMM_OK or GEMM_ERR_CUDA / GEMM_ERR_MISALIGNED.

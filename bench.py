@@ -54,7 +54,7 @@ FLUSH_BYTES = 256 << 20              # > 2x the 126 MiB L2
 # BF16: stages 0 and tile 0 take the library's choice for the workload (at
 # 8192^3 the 256-row tile with three stages); the plan resolves both before
 # anything is timed, so the JSON line names what ran.
-DEFAULT_LEG = {"f32": dict(fill="tma", stages=4, tile=128), "bf16": dict(fill="tma", stages=0, tile=0)}
+DEFAULT_LEG = {"f32": dict(fill="tma", stages=2, tile=128), "bf16": dict(fill="tma", stages=0, tile=0)}
 
 
 # --------------------------------------------------------------------- dist
@@ -838,12 +838,18 @@ def run_ours(args, dist: Dist):
         e2e = {"value": dist.world * flops / (e_total / e_steps / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": dist.world * int(Ah.element_size() * M * K + Bh.element_size() * K * N),
                "d2h_bytes_per_step": dist.world * int(4 * M * N), "ms_per_step": e_total / e_steps}
-        # The GEMM launches of the host path's row chunks, every step.
+        # The GEMM launches of the host path, every step: BF16 row chunks; for
+        # FP32 the executor's K steps over all rows and the last step's row
+        # chunks (device copies at 16-byte row pitches).
         if is_bf16:
-            per_step = len(pg.host_row_chunks(M))
+            per_step = len(pg.host_row_chunks(M, N, num_sms))
         else:
-            per_step = sum(f32_kernels_per_call(pg, r1 - r0, N, K, K, N, leg["fill"], leg["stages"], leg["tile"])
-                           for r0, r1 in pg.host_row_chunks(M))
+            kb, rb = pg.host_schedule_f32(M, N, K, num_sms)
+            calls = [(M, k1 - k0) for k0, k1 in zip(kb[:-2], kb[1:-1])]
+            calls += [(r1 - r0, kb[-1] - kb[-2]) for r0, r1 in zip(rb, rb[1:])]
+            lda_d, ldb_d = -(-max(K, 1) // 4) * 4, -(-max(N, 1) // 4) * 4
+            per_step = sum(f32_kernels_per_call(pg, m, N, k, lda_d, ldb_d, leg["fill"], leg["stages"], leg["tile"])
+                           for m, k in calls)
         launches_e2e = e_steps * per_step
 
     kernel_key = f"{name}:{leg['fill']}/S{leg['stages']}/T{leg['tile']}"

@@ -100,13 +100,27 @@ enum gemm_fill_mode {
  * are not 16-byte aligned (so copied 4 bytes at a time) returns
  * GEMM_ERR_UNSUPPORTED: the 4-byte copies take the prefetch size only.
  */
+/*
+ * GEMM_OPT_ACCUMULATE (FP32 only; gemm_bf16 returns GEMM_ERR_UNSUPPORTED):
+ * C = C + A·B with each element's FMA chain starting from the value C holds
+ * instead of +0: C's value, then one fused multiply-add per k, ascending.
+ * If C holds the result of an earlier call over the first K0 columns of A
+ * and rows of B, a call over the remaining columns and rows with this
+ * option gives, bit for bit, what one call over all of them gives.  The
+ * pages have no counterpart: the host-buffer path uses it to start on the
+ * first rows of C while B is still arriving in row blocks.  With K = 0 the
+ * call leaves C as it is.  It does not combine with the cache qualifiers
+ * above (GEMM_ERR_UNSUPPORTED).  A starting value of -0 may come out as +0 where
+ * a zero-filled K tail adds +0 to it; a chain started from +0 never holds -0.
+ */
 enum gemm_fill_option {
     GEMM_OPT_L2_PREFETCH_128B = 0x100,
     GEMM_OPT_A_EVICT_FIRST = 0x200,
     GEMM_OPT_A_EVICT_LAST = 0x400,
     GEMM_OPT_B_EVICT_FIRST = 0x800,
     GEMM_OPT_B_EVICT_LAST = 0x1000,
-    GEMM_OPT_MASK = 0x1F00
+    GEMM_OPT_ACCUMULATE = 0x2000,
+    GEMM_OPT_MASK = 0x3F00
 };
 
 typedef enum gemm_status {
@@ -148,7 +162,8 @@ typedef struct gemm_plan {
  * gemm_f32: C[M x N] = A[M x K] * B[K x N], float32 in and out.
  *
  *   M, N, K     logical sizes, >= 0.  M == 0 or N == 0 is a no-op; K == 0
- *               writes zeros to C (an empty sum).
+ *               writes zeros to C (an empty sum), or with
+ *               GEMM_OPT_ACCUMULATE leaves C as it is.
  *   A, lda      device pointer, leading dimension >= max(K, 1).
  *   B, ldb      device pointer, leading dimension >= max(N, 1).
  *   C, ldc      device pointer, leading dimension >= max(N, 1).  Only the
@@ -156,9 +171,11 @@ typedef struct gemm_plan {
  *               left untouched.
  *   fill_mode   GEMM_FILL_SYNC, GEMM_FILL_CPASYNC, GEMM_FILL_TMA,
  *               GEMM_FILL_CPASYNC_MBAR or GEMM_FILL_CPASYNC_WS, optionally
- *               OR-ed with GEMM_OPT_* cache qualifiers.
+ *               OR-ed with GEMM_OPT_* cache qualifiers and
+ *               GEMM_OPT_ACCUMULATE (C = C + A·B).
  *   stages      sync: 0 or 1.  Others: 2..6, or 0 for the default: 4, or 2
- *               for GEMM_FILL_CPASYNC_WS.
+ *               for GEMM_FILL_CPASYNC_WS and for GEMM_FILL_TMA on the
+ *               128x128 tile.
  *               Each stage is one more slice in flight
  *               and one more copy of both tiles in shared memory (day 74,
  *               "Exercise").
@@ -249,6 +266,76 @@ int gemm_f32_noalloc(int M, int N, int K,
                      float *C, int ldc,
                      int fill_mode, int stages, int block_tile,
                      void *stream);
+
+/*
+ * gemm_f32_host: C = A·B in FP32 with A, B and C in HOST memory (page-locked
+ * for the copies to overlap; pageable memory works but each copy then waits
+ * for the host).  The pages measure device-resident operands; this entry
+ * point is the library's own host-buffer path, not a counterpart of theirs.
+ *
+ *   M, N, K, fill_mode, stages, block_tile
+ *               as gemm_f32 (block_tile 0 picks the whole problem's tile).
+ *               GEMM_OPT_ACCUMULATE in fill_mode is refused: the executor
+ *               uses it itself.
+ *   A, B, C     host pointers, 4-byte aligned; only the M x N logical
+ *               elements of C are written.
+ *   lda, ldb, ldc  row pitches in floats, at least max(K, 1), max(N, 1),
+ *               max(N, 1).  Any pitch works for every fill: the GEMMs read
+ *               device copies laid out at 16-byte row pitches.
+ *   scratch     device memory of at least gemm_f32_host_scratch() bytes,
+ *               256-byte aligned, owned by the caller: device copies of A,
+ *               B and C and the K-split hand-over spaces.  Nothing in it
+ *               needs clearing, and it may be reused by the next call.
+ *   status_out  host pointer or NULL.  If given, the call's last step
+ *               copies the device status word there and clears it (as
+ *               gemm_device_status does, without synchronising): once
+ *               `stream` has reached the end of the call, *status_out is 0
+ *               or the family | role word of the first bounded wait that
+ *               gave up, in which case C is undefined.  Page-locked memory
+ *               keeps that copy asynchronous.
+ *   stream      the call starts after the work already on `stream`, and
+ *               `stream` waits for its end; it returns without waiting.
+ *               A, B, C, scratch and status_out must stay valid, and A and
+ *               B unchanged, until `stream` has reached that point.
+ *
+ * Work runs on three streams the library makes per device and context
+ * (copies in, GEMMs, copies out), ordered by events: B's rows and A's
+ * columns cross the link in K blocks, each block's GEMM over all rows
+ * starts as soon as it has landed and continues every element's FMA chain
+ * from the previous block's C (GEMM_OPT_ACCUMULATE), and the last block runs
+ * in row chunks, each copied out as soon as it is done (K under 2048: one
+ * block, with A moved chunk by chunk).  Its blocks: 512, then up to 2048
+ * each, the last 2048 or a little more; its row chunks: about two waves of
+ * 128x128 tiles each, the last about one (gemm_f32_host_schedule).  The result is bit-identical to
+ * gemm_f32 on the same fill.  Calls on one device are serialised: each
+ * starts after the previous one has finished on the GPU.  Kernel timeouts
+ * are recorded in the status word as for gemm_f32 (see status_out).
+ * Returns GEMM_OK or an error (GEMM_ERR_INVALID_ARG for a missing or small
+ * scratch, GEMM_ERR_MISALIGNED for a misaligned one); after an error some
+ * work may already be enqueued, and `stream` still waits for it.
+ */
+int gemm_f32_host(int M, int N, int K,
+                  const float *A, int lda,
+                  const float *B, int ldb,
+                  float *C, int ldc,
+                  int fill_mode, int stages, int block_tile,
+                  void *scratch, size_t scratch_bytes,
+                  unsigned int *status_out,
+                  void *stream);
+
+/* gemm_f32_host_scratch: device bytes gemm_f32_host needs for these sizes on
+ * the current device (*bytes, a host pointer).  No device memory is touched. */
+int gemm_f32_host_scratch(int M, int N, int K, size_t *bytes);
+
+/* gemm_f32_host_schedule: the cut gemm_f32_host makes for these sizes on
+ * `sms` SMs, without touching the device: K-block bounds k_bounds[0..*n_k]
+ * (0 = k_bounds[0] < ... < k_bounds[*n_k] = K) and the row-chunk bounds of
+ * the last block, row_bounds[0..*n_rows] (0 ... M).  k_cap and row_cap are
+ * the arrays' lengths; GEMM_ERR_INVALID_ARG if either is too short (17 and
+ * 65 always suffice). */
+int gemm_f32_host_schedule(int M, int N, int K, int sms,
+                           int *k_bounds, int k_cap, int *n_k,
+                           int *row_bounds, int row_cap, int *n_rows);
 
 /* gemm_f32_plan: validate exactly as gemm_f32 does and describe the launch it
  * would make, without touching the device.  `plan` is a host pointer. */

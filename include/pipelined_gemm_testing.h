@@ -64,6 +64,28 @@ int gemm_testing_withhold_handover(int on);
  */
 int gemm_testing_f32_piece(int tiles, int ctas, int k_slices, int split, int cta, int idx, int *out);
 
+/*
+ * gemm_testing_host_policy: override the constants of gemm_f32_host's
+ * schedule for later calls (0 keeps a constant's default): the first and
+ * last K block, the longest block between them, the shortest K cut into
+ * blocks, and the rows of the last and of the other row chunks in hundredths
+ * of a wave of 128 x 128 tiles.  Block lengths are rounded up to multiples
+ * of 16.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for a negative value or
+ * a block under 16.  For schedule sweeps and tests only.
+ */
+int gemm_testing_host_policy(int k_first, int k_last, int k_mid_max, int k_steps_min,
+                             int last_rows_waves100, int rows_waves100);
+
+/*
+ * gemm_testing_host_streams: how many GEMM streams gemm_f32_host uses (1 to
+ * 3; with more than one, row chunk i's GEMMs of every K step run on stream
+ * i mod n, so kernels of different chunks can share the GPU), and whether
+ * its GEMMs split their last round of tiles in K (1) or not (0).  0 and -1
+ * restore the defaults.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG.  For
+ * schedule sweeps and tests only.
+ */
+int gemm_testing_host_streams(int comp_streams, int split);
+
 #ifdef __cplusplus
 }
 #endif

@@ -77,11 +77,17 @@ def test_plan_defaults_and_shapes(lib):
     # when no device can be asked) + 112 leave a last round to split, done by
     # one persistent CTA per SM whose hand-over space is one 64 KiB
     # accumulator tile and an 8-byte flag per CTA.
+    # Its default ring depth is two stages (four for every other ring fill
+    # and tile).
     st, p = _plan(4096, 4096, 4096, fill=2)
-    assert st == 0 and p["block_m"] == 128 and p["stages"] == 4 and p["threads"] == 288
+    assert st == 0 and p["block_m"] == 128 and p["stages"] == 2 and p["threads"] == 288
     assert (p["grid_x"], p["grid_y"], p["k_slices"]) == (32, 32, 256)
     assert p["persistent_ctas"] == 152 and p["workspace_bytes"] == 152 * (65536 + 8)
-    assert p["smem_bytes"] == 4 * 16384 + 16 * 4 + 64 + 1024
+    assert p["smem_bytes"] == 2 * 16384 + 16 * 2 + 64 + 1024
+    st, p = _plan(4096, 4096, 4096, fill=2, stages=4)
+    assert st == 0 and p["stages"] == 4 and p["smem_bytes"] == 4 * 16384 + 16 * 4 + 64 + 1024
+    st, p = _plan(1024, 1024, 1024, fill=2)  # automatic 64 tile
+    assert st == 0 and p["block_m"] == 64 and p["stages"] == 4
     st, p = _plan(152 * 128, 2 * 128, 256, fill=2)  # 304 tiles: whole rounds, nothing to split
     assert st == 0 and p["persistent_ctas"] == 0 and p["workspace_bytes"] == 0
     st, p = _plan(1024, 1024, 4096, fill=2, tile=128)  # 64 tiles: one round, fewer CTAs than SMs
@@ -260,8 +266,27 @@ def test_cache_options_bf16_and_unknown_bits(lib):
         with pytest.raises(pg.GemmError):
             pg.plan_bf16(256, 256, 256, fill=fill, options=opts)
     plan = pg.GemmPlan()
-    assert lib.gemm_f32_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2 | 0x2000, 2, 0, ctypes.byref(plan)) == 1
+    assert lib.gemm_f32_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2 | 0x4000, 2, 0, ctypes.byref(plan)) == 1
     assert lib.gemm_f32_plan(64, 64, 64, 256, 64, 256, 64, 256, 64, 2 | 0x80, 2, 0, ctypes.byref(plan)) == 1
+
+
+def test_accumulate_option_fp32_only(lib):
+    """GEMM_OPT_ACCUMULATE: every FP32 fill takes it (alone or beside cache
+    options) and the plan reports it; the BF16 path refuses it as
+    unsupported."""
+    for fill in ("sync", "cpasync", "tma", "cpasync_mbar", "cpasync_ws"):
+        plan = pg.GemmPlan()
+        code = pg.FILL[fill] | pg.OPT_ACCUMULATE
+        assert lib.gemm_f32_plan(300, 200, 100, 256, 100, 256, 200, 256, 200, code, 0, 0, ctypes.byref(plan)) == 0
+        assert plan.options == pg.OPT_ACCUMULATE
+    # the kernels that start from C are built with plain copies only
+    plan = pg.GemmPlan()
+    for fill, opt in (("tma", 0x1000), ("cpasync", 0x100), ("cpasync_ws", 0x200), ("cpasync_mbar", 0x800)):
+        assert lib.gemm_f32_plan(256, 256, 256, 256, 256, 256, 256, 256, 256,
+                                 pg.FILL[fill] | opt | pg.OPT_ACCUMULATE, 4, 0, ctypes.byref(plan)) == 3
+    for fill in ("tma", "cpasync", "sync"):
+        assert lib.gemm_bf16_plan(256, 256, 256, 256, 256, 256, 256, 256, 256, pg.FILL[fill] | pg.OPT_ACCUMULATE, 0,
+                                  0, ctypes.byref(plan)) == 3
 
 
 def _pieces(lib, tiles, ctas, k, split):

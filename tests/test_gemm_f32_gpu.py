@@ -264,17 +264,18 @@ def test_non_default_stream():
 
 @pytest.mark.parametrize("fill", ["sync", "tma"])
 def test_host_tensors_chunked_match_device_path(fill):
-    """A host call split into more row chunks than it has streams (so every
-    stream runs several chunks, the last one ragged) gives the same bits as
-    one device call."""
+    """A host call (the native executor, one K block at this K) split into
+    several row chunks, the last one ragged, gives the same bits as one
+    device call."""
     import torch
     import async_copy_pipelined_gb300 as pg
-    M, N, K = 3300, 384, 256
+    M, N, K = 3300, 4096, 256
     A, B = f32_operands("uniform", M, N, K, seed=10, fill="tma")
     Ah = torch.from_numpy(A).pin_memory()[:, :K]
     Bh = torch.from_numpy(B).pin_memory()[:, :N]
-    chunks = pg.host_row_chunks(M)
-    assert len(chunks) > pg.HOST_STREAMS and (chunks[-1][1] - chunks[-1][0]) % 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    kb, rb = pg.host_schedule_f32(M, N, K, sms)
+    assert kb == [0, K] and len(rb) > 3 and (rb[-1] - rb[-2]) % 128
     Ch = pg.gemm_f32(Ah, Bh, fill=fill)
     Cd = pg.gemm_f32(torch.from_numpy(A).cuda()[:, :K], torch.from_numpy(B).cuda()[:, :N], fill=fill)
     assert torch.equal(Ch.view(torch.int32), Cd.cpu().view(torch.int32))
