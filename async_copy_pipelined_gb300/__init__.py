@@ -106,7 +106,7 @@ def _bind(l):
     l.gemm_f32_host_schedule.restype = I
     l.gemm_testing_host_policy.argtypes = [I, I, I, I, I, I]
     l.gemm_testing_host_policy.restype = I
-    l.gemm_testing_host_streams.argtypes = [I, I]
+    l.gemm_testing_host_streams.argtypes = [I, I, I]
     l.gemm_testing_host_streams.restype = I
     return l
 

@@ -57,11 +57,13 @@ struct HostPolicy {
     int rows_waves100 = 200;      // other row chunks: about two waves
     int comp_streams = 1;         // GEMM streams; with more than one, every step runs per row chunk
     int split = 1;                // K-split of the last round of tiles (hand-over workspace)
+    int round_chunks = 1;         // first row chunks a whole number of rounds of tiles on the SMs
 };
 
 std::atomic<int> g_policy[6] = {{0}, {0}, {0}, {0}, {0}, {0}}; // test overrides, 0: default
 std::atomic<int> g_comp_streams{0};                                // test override, 0: default
 std::atomic<int> g_split{-1};                                      // test override, -1: default
+std::atomic<int> g_round_chunks{-1};                               // test override, -1: default
 
 HostPolicy policy()
 {
@@ -76,6 +78,8 @@ HostPolicy policy()
         p.comp_streams = g_comp_streams.load();
     if (g_split.load() >= 0)
         p.split = g_split.load();
+    if (g_round_chunks.load() >= 0)
+        p.round_chunks = g_round_chunks.load();
     return p;
 }
 
@@ -145,13 +149,43 @@ rows:
         s.r[++s.n_r] = M;
         return s;
     }
-    long long parts = (rest + big_rows - 1) / big_rows;
-    if (parts > kMaxRowChunks - 1)
-        parts = kMaxRowChunks - 1;
-    const long long rows = round_up((rest + parts - 1) / parts, 128);
-    for (long long b = rows; b < rest; b += rows)
+    // A chunk whose tiles fill whole rounds of SMs runs in the one-tile
+    // kernel alone, faster than the split schedule's persistent kernel: with
+    // round_chunks the first chunk is the largest such block of rows of at
+    // most two usual chunks, if there is one.
+    long long start = 0;
+    if (pol.round_chunks) {
+        long long g = sms, t = tiles_n; // gcd
+        while (t != 0) {
+            const long long r = g % t;
+            g = t;
+            t = r;
+        }
+        const long long unit = sms / g * 128; // rows of a whole number of rounds
+        // at most two usual chunks' worth, so that its copy out still
+        // overlaps the GEMMs of the chunks after it
+        const long long cap = rest < 2 * big_rows ? rest : 2 * big_rows;
+        const long long fit = cap / unit * unit;
+        if (fit >= unit && fit >= big_rows && fit < rest) {
+            s.r[++s.n_r] = static_cast<int>(fit);
+            start = fit;
+        }
+    }
+    if (start == rest) {
+        s.r[++s.n_r] = M;
+        return s;
+    }
+    // The rows between: `parts` chunks of whole 128-row tiles, as equal as
+    // the tile rows allow.
+    long long parts = (rest - start + big_rows - 1) / big_rows;
+    if (parts > kMaxRowChunks - 2)
+        parts = kMaxRowChunks - 2;
+    const long long tile_rows = (rest - start) / 128;
+    long long b = start;
+    for (long long i = 0; i < parts; ++i) {
+        b += (tile_rows / parts + (i < tile_rows % parts ? 1 : 0)) * 128;
         s.r[++s.n_r] = static_cast<int>(b);
-    s.r[++s.n_r] = static_cast<int>(rest);
+    }
     s.r[++s.n_r] = M;
     return s;
 }
@@ -270,12 +304,14 @@ extern "C" int gemm_testing_host_policy(int k_first, int k_last, int k_mid_max, 
     return GEMM_OK;
 }
 
-extern "C" int gemm_testing_host_streams(int comp_streams, int split)
+extern "C" int gemm_testing_host_streams(int comp_streams, int split, int round_chunks)
 {
-    if (comp_streams < 0 || comp_streams > kMaxCompStreams || split < -1 || split > 1)
+    if (comp_streams < 0 || comp_streams > kMaxCompStreams || split < -1 || split > 1 || round_chunks < -1 ||
+        round_chunks > 1)
         return GEMM_ERR_INVALID_ARG;
     g_comp_streams.store(comp_streams);
     g_split.store(split);
+    g_round_chunks.store(round_chunks);
     return GEMM_OK;
 }
 

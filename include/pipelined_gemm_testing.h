@@ -79,12 +79,14 @@ int gemm_testing_host_policy(int k_first, int k_last, int k_mid_max, int k_steps
 /*
  * gemm_testing_host_streams: how many GEMM streams gemm_f32_host uses (1 to
  * 3; with more than one, row chunk i's GEMMs of every K step run on stream
- * i mod n, so kernels of different chunks can share the GPU), and whether
- * its GEMMs split their last round of tiles in K (1) or not (0).  0 and -1
- * restore the defaults.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG.  For
- * schedule sweeps and tests only.
+ * i mod n, so kernels of different chunks can share the GPU), whether its
+ * GEMMs split their last round of tiles in K (1) or not (0), and whether
+ * its first row chunk is the largest block of rows whose tiles fill whole
+ * rounds of SMs (1) or not (0).  0, -1 and -1 restore the defaults.
+ * Returns GEMM_OK or GEMM_ERR_INVALID_ARG.  For schedule sweeps and tests
+ * only.
  */
-int gemm_testing_host_streams(int comp_streams, int split);
+int gemm_testing_host_streams(int comp_streams, int split, int round_chunks);
 
 #ifdef __cplusplus
 }

@@ -54,10 +54,21 @@ def test_f32_host_schedule_covers_k_and_rows_once(M, N, K):
 
 def test_f32_host_schedule_rows_follow_waves():
     """At N = 4096 on 152 SMs one wave of 128 x 128 tiles is 5 tile rows
-    (640 rows): the last chunk is one wave, the others about two."""
+    (640 rows): the last chunk is one wave, the others about two, and the
+    first is 19 tile rows (608 tiles, exactly four rounds of 152), the
+    largest whole-round block of at most two usual chunks."""
     kb, rb = pg.host_schedule_f32(4096, 4096, 4096, 152)
     assert kb == [0, 512, 2048, 4096]
-    assert rb == [0, 1152, 2304, 3456, 4096]
+    assert rb == [0, 2432, 3456, 4096]
+    assert pg.lib().gemm_testing_host_streams(0, -1, 0) == 0
+    try:
+        assert pg.host_schedule_f32(4096, 4096, 4096, 152)[1] == [0, 1152, 2304, 3456, 4096]
+    finally:
+        assert pg.lib().gemm_testing_host_streams(0, -1, -1) == 0
+    # chunks between the first and the last differ by at most one tile row
+    rb = pg.host_schedule_f32(8192, 8192, 8192, 152)[1]
+    sizes = [b - a for a, b in zip(rb[:-2], rb[1:-1])]
+    assert max(sizes) - min(sizes) <= 128 and rb[-1] - rb[-2] >= 384
 
 
 def test_f32_host_policy_hook_and_scratch():
@@ -84,8 +95,8 @@ def test_f32_host_policy_hook_and_scratch():
     # device copies of A, B and C, then one hand-over space per GEMM stream (up to 3)
     assert need.value == c + 3 * up(sms * (128 * 128 * 4 + 8))
     assert lib.gemm_f32_host_scratch(-1, 1, 1, ctypes.byref(need)) == 1
-    assert lib.gemm_testing_host_streams(4, 1) == 1 and lib.gemm_testing_host_streams(1, 2) == 1
-    assert lib.gemm_testing_host_streams(0, -1) == 0
+    assert lib.gemm_testing_host_streams(4, 1, 1) == 1 and lib.gemm_testing_host_streams(1, 2, 1) == 1
+    assert lib.gemm_testing_host_streams(0, -1, -1) == 0
 
 
 def test_fp32_peak_is_sms_times_lanes_times_clock():

@@ -65,7 +65,7 @@ def test_several_gemm_streams(small_policy, streams, split, M, N, K):
     chunk), with and without the K split of the last round: same bits."""
     pg = small_policy
     lib = pg.lib()
-    assert lib.gemm_testing_host_streams(streams, split) == 0
+    assert lib.gemm_testing_host_streams(streams, split, -1) == 0
     try:
         A, B = f32_operands("uniform", M, N, K, seed=76, fill="tma")
         want = oracle.gemm_fmaf_chain(A, B, M, N, K)
@@ -73,7 +73,7 @@ def test_several_gemm_streams(small_policy, streams, split, M, N, K):
             C = pg.gemm_f32(_host(A, K), _host(B, N), fill=fill)
             assert_bitwise_equal(C.numpy(), want, f"{streams} GEMM streams, split {split}, {fill}")
     finally:
-        assert lib.gemm_testing_host_streams(0, -1) == 0
+        assert lib.gemm_testing_host_streams(0, -1, -1) == 0
 
 
 def test_strided_and_pageable_host_buffers(small_policy):
