@@ -442,13 +442,14 @@ extern "C" int gemm_f32_host(int M, int N, int K, const float *A, int lda, const
         return true;
     };
     if (st == GEMM_OK && S.n_k == 1) {
-        // One step: all of B, then A, the GEMM and C chunk by chunk.
-        if (!copy_b(0, K))
+        // One step: all of B, then A, the GEMM and C chunk by chunk (K = 0:
+        // nothing to copy in; the GEMMs write the empty sum's zeros).
+        if (K > 0 && !copy_b(0, K))
             st = GEMM_ERR_CUDA;
         for (int i = 0; st == GEMM_OK && i < S.n_r; ++i) {
             const int r0 = S.r[i], r1 = S.r[i + 1];
             cudaStream_t cs = comp_of(i);
-            if (!copy_a(r0, r1, 0, K) || !join(H.h2d, cs))
+            if ((K > 0 && !copy_a(r0, r1, 0, K)) || !join(H.h2d, cs))
                 st = GEMM_ERR_CUDA;
             else if ((st = gemm(cs, r0, r1, 0, K, false)) == GEMM_OK && (!join(cs, H.d2h) || !copy_c(r0, r1)))
                 st = GEMM_ERR_CUDA;

@@ -135,6 +135,8 @@ def test_kernel_sources_sha_covers_every_source(tmp_path, monkeypatch):
     (csrc / "b.cuh").write_text("y")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h1 = bench.kernel_sources_sha()
+    (csrc / "host_exec.cu").write_text("w")  # sequences calls only: not hashed
+    assert bench.kernel_sources_sha() == h1
     (csrc / "b.cuh").write_text("z")
     assert bench.kernel_sources_sha() != h1
 

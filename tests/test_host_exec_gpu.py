@@ -76,6 +76,20 @@ def test_several_gemm_streams(small_policy, streams, split, M, N, K):
         assert lib.gemm_testing_host_streams(0, -1, -1) == 0
 
 
+@pytest.mark.parametrize("M,N,K", [(5, 3, 0), (1, 1, 1), (130, 7, 3), (129, 200, 17), (0, 5, 5), (5, 0, 5)])
+def test_tiny_and_empty_shapes(M, N, K):
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    A = np.random.default_rng(78).uniform(-1, 1, size=(M, K)).astype(np.float32)
+    B = np.random.default_rng(79).uniform(-1, 1, size=(K, N)).astype(np.float32)
+    C = pg.gemm_f32(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), fill="tma")
+    assert tuple(C.shape) == (M, N)
+    if M and N and K:
+        assert_bitwise_equal(C.numpy(), oracle.gemm_fmaf_chain(A, B, M, N, K), f"host executor {M}x{N}x{K}")
+    elif M and N:  # the empty sum: +0 everywhere
+        assert np.all(C.numpy().view(np.uint32) == 0)
+
+
 def test_strided_and_pageable_host_buffers(small_policy):
     """Host A and B with row pitches beyond their widths (2-D copies), a host
     C with ldc > N whose extra columns must keep their sentinel, and
