@@ -98,6 +98,8 @@ def _bind(l):
     l.gemm_testing_f32_piece.argtypes = [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)]
     l.gemm_testing_f32_piece.restype = I
     l.gemm_f32_host.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P, P]
+    l.gemm_bf16_ws.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P]
+    l.gemm_bf16_ws.restype = I
     l.gemm_f32_host.restype = I
     l.gemm_f32_host_scratch.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_size_t)]
     l.gemm_f32_host_scratch.restype = I
@@ -462,14 +464,21 @@ def gemm_f32(A, B, C=None, *, fill="tma", stages=0, block_tile=0, stream=None, o
     return C
 
 
-def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, options=()):
+def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, options=(), workspace=None):
     """C (float32) = A @ B for bfloat16 A (M x K), B (K x N) on the tensor cores.
 
     fill: "tma" (default), "cpasync" or "sync" fills the shared-memory stages
     the MMAs read; block_m: 128 or 256 rows per CTA tile, 0 to let the
-    library choose.  Every fill and tile gives the same bits.  Host tensors
-    and the device status word are handled as in gemm_f32: on the device
-    path, check device_status() before trusting C."""
+    library choose.  Every fill and tile gives the same bits.  workspace:
+    hand-over space for the TMA fill's K split of the last round of tiles
+    (gemm_bf16_ws in the C header), as for gemm_f32: None (the default: no
+    split), "auto" or a uint8 CUDA tensor; the bits are the same either
+    way.  The split is off by default because on GB300 it measured slower
+    than the unsplit kernel at 8192^3 (603 against 584 us on the 256-row
+    tile): its extra accumulator drains cost more than the idle SMs of the
+    partial last round.  Host
+    tensors and the device status word are handled as in gemm_f32: on the
+    device path, check device_status() before trusting C."""
     import torch
     dev = _operand_device(A, B, C, stream)
     if not A.is_cuda:
@@ -485,7 +494,7 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, opt
             except (RuntimeError, ValueError):
                 pass  # the chunk calls report the error
         return _host_roundtrip(lambda a, b, c, s: gemm_bf16(a, b, c, fill=fill, stages=stages, block_m=block_m,
-                                                            stream=s, options=options),
+                                                            stream=s, options=options, workspace=workspace),
                                A, B, C, torch.float32)
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("gemm_bf16 takes bfloat16 tensors")
@@ -499,9 +508,20 @@ def gemm_bf16(A, B, C=None, *, fill="tma", stages=0, block_m=0, stream=None, opt
     if (Mc, Nc) != (M, N) or C.dtype != torch.float32:
         raise ValueError("C must be a float32 M x N tensor")
     _refuse_aliased_output(C, A, B)
+    code = _fill_code(fill, options)
     with torch.cuda.device(dev):
-        st = lib().gemm_bf16(M, N, K, pa, lda, pb, ldb, pc, ldc, _fill_code(fill, options), stages, block_m,
-                             _stream_handle(stream))
+        sh = _stream_handle(stream)
+        ws_ptr, ws_bytes = None, 0
+        if workspace is not None:
+            plan = GemmPlan()
+            st = lib().gemm_bf16_plan(M, N, K, pa, lda, pb, ldb, pc, ldc, code, stages, block_m, ctypes.byref(plan))
+            _check(st, "gemm_bf16_plan")
+            if plan.workspace_bytes > 0:
+                ws = _workspace(dev, sh.value or 0, plan.workspace_bytes) if isinstance(workspace, str) else workspace
+                if ws.device != dev:
+                    raise ValueError(f"workspace is on {ws.device}, operands on {dev}")
+                ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+        st = lib().gemm_bf16_ws(M, N, K, pa, lda, pb, ldb, pc, ldc, code, stages, block_m, ws_ptr, ws_bytes, sh)
     _check(st, "gemm_bf16")
     return C
 

@@ -504,6 +504,18 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
     const long long tiles_n = (N + kBf16BlockN - 1) / kBf16BlockN;
     if (tiles_m * tiles_n > 0x7fffffffLL)
         return GEMM_ERR_INVALID_ARG;
+    // The TMA fill, like the FP32 one, can split the last round of tiles and
+    // one more in K between the persistent CTAs (gemm_bf16_ws): hand-over
+    // space of one block_m x 256 FP32 accumulator tile and an 8-byte flag
+    // per CTA.
+    long long handover = 0;
+    if (fill == GEMM_FILL_TMA && work && K > 0) {
+        const int sms = planning_sms();
+        const F32Schedule sch = F32Schedule::make(static_cast<int>(tiles_m * tiles_n), sms,
+                                                  (K + kBf16BlockK - 1) / kBf16BlockK, true);
+        if (sch.split())
+            handover = static_cast<long long>(sms) * (static_cast<long long>(block_m) * kBf16BlockN * 4 + 8);
+    }
     if (plan) {
         std::memset(plan, 0, sizeof *plan);
         plan->fill_mode = fill;
@@ -521,7 +533,7 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         plan->options = fill_mode & GEMM_OPT_MASK;
         plan->persistent_ctas = static_cast<int>(tiles_m * tiles_n < planning_sms() ? tiles_m * tiles_n
                                                                                     : planning_sms());
-        plan->workspace_bytes = 0;
+        plan->workspace_bytes = static_cast<int>(handover);
     }
     if (args) {
         args->M = M;
@@ -545,6 +557,10 @@ static int plan_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint
         args->num_sms = 0;
         args->device = 0;
         args->ctx = 0;
+        args->handover = nullptr; // set when the call brings hand-over space
+        args->handover_bytes = handover;
+        args->epoch = 0;
+        args->withhold_handover = g_hook_withhold_handover.load();
     }
     return GEMM_OK;
 }
@@ -660,10 +676,24 @@ int gemm_bf16_plan(int M, int N, int K, const uint16_t *A, int lda, const uint16
 int gemm_bf16(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
               int fill_mode, int stages, int block_m, void *stream)
 {
+    return gemm_bf16_ws(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_m, nullptr, 0, stream);
+}
+
+int gemm_bf16_ws(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
+                 int fill_mode, int stages, int block_m, void *workspace, size_t workspace_bytes, void *stream)
+{
     Bf16Args args;
     int st = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, fill_mode, stages, block_m, nullptr, &args);
     if (st != GEMM_OK)
         return st;
+    if (workspace != nullptr && args.handover_bytes > 0) {
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+            return GEMM_ERR_MISALIGNED;
+        if (workspace_bytes < static_cast<size_t>(args.handover_bytes))
+            return GEMM_ERR_INVALID_ARG;
+        args.handover = workspace;
+        args.epoch = next_epoch();
+    }
     int dev;
     st = check_device(&dev);
     if (st != GEMM_OK)

@@ -71,6 +71,7 @@
 #include <cstring>
 #include <type_traits>
 
+#include "f32_schedule.cuh"
 #include "gemm_internal.h"
 #include "ptx.cuh"
 #include "tma_ring.cuh"
@@ -233,7 +234,12 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
     const uint32_t tmem_empty0 = tmem_full0 + 16u; // [kAccBufs]
     const uint32_t epi_done = tmem_empty0 + 16u;
     const uint32_t mma_done = epi_done + 8u;
-    const uint32_t tmem_slot = mma_done + 8u;
+    // K split (each used at most once per CTA): the epilogue warps have put
+    // the previous CTA's accumulators into tensor memory / have written this
+    // CTA's accumulators to the hand-over space.
+    const uint32_t acc_loaded = mma_done + 8u;
+    const uint32_t handover_written = acc_loaded + 8u;
+    const uint32_t tmem_slot = handover_written + 8u;
     volatile uint32_t *tmem_slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x / 32;
@@ -242,6 +248,19 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
     const int tiles_n = (p.N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
     const int k_blocks = (p.K + BK - 1) / BK;
+    // The pieces this CTA computes (f32_schedule.cuh): without a split, the
+    // tiles blockIdx.x, + gridDim.x, ... whole; with one (TMA fill and
+    // hand-over space), the whole rounds but the last, then its share of the
+    // rest as head, whole tiles and tail.
+    const bool split = Fill == GEMM_FILL_TMA && p.handover != nullptr;
+    const F32CtaPieces work = F32CtaPieces::make(
+        F32Schedule::make(num_tiles, static_cast<int>(gridDim.x), k_blocks, split), static_cast<int>(blockIdx.x));
+    const int pieces = work.count();
+    const int cta = static_cast<int>(blockIdx.x);
+    constexpr int kHandoverQuads = BM * BN / 4; // 16-byte units of one CTA's hand-over slot
+    uint4 *handover_slots = static_cast<uint4 *>(p.handover);
+    unsigned long long *handover_flags = reinterpret_cast<unsigned long long *>(
+        static_cast<uint8_t *>(p.handover) + static_cast<size_t>(gridDim.x) * kHandoverQuads * 16u);
 
     if (threadIdx.x == 0) {
         ring.init(1, R::kFullArrivals);
@@ -251,6 +270,8 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
         }
         mbar_init(epi_done, T::kEpiWarps);
         mbar_init(mma_done, 1);
+        mbar_init(acc_loaded, T::kEpiWarps);
+        mbar_init(handover_written, T::kEpiWarps);
         fence_barrier_init();
     }
     if (warp == R::kMmaWarp) {
@@ -272,10 +293,11 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
             const uint64_t pol_a = hint ? l2_policy(p.pol_a) : 0, pol_b = hint ? l2_policy(p.pol_b) : 0;
             int f = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int idx = 0; idx < pieces && ok; ++idx) {
+                const F32Piece pc = work.piece(idx);
                 int mb, nb;
-                tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
-                for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                tile_coords<MH>(pc.tile, tiles_m, tiles_n, mb, nb);
+                for (int kb = pc.s_begin; kb < pc.s_end; ++kb, ++f) {
                     if (f == p.withhold)
                         continue; // test hook: this position is never filled
                     if (!ring.producer_acquire(f, p.wait_limit_ns)) {
@@ -460,18 +482,24 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int f = 0;
-            int local = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            for (int local = 0; local < pieces && ok; ++local) {
+                const F32Piece pc = work.piece(local);
                 const int slot = local % T::kAccBufs;
                 const uint32_t use_parity = static_cast<uint32_t>((local / T::kAccBufs) & 1);
                 if (!mbar_wait_bounded(tmem_empty0 + 8u * slot, use_parity ^ 1u, p.wait_limit_ns)) {
                     record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
                     break;
                 }
+                // A tail continues from the accumulators the epilogue warps
+                // have put into this slot.
+                if (pc.from_partial && !mbar_wait_bounded(acc_loaded, 0, p.wait_limit_ns)) {
+                    record_error(p.status, kErrFamilyBf16 | kErrRoleHandover);
+                    break;
+                }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * MH * BN);
-                for (int kb = 0; kb < k_blocks; ++kb, ++f) {
+                for (int kb = pc.s_begin; kb < pc.s_end; ++kb, ++f) {
                     if (!ring.consumer_wait(f, p.wait_limit_ns)) {
                         record_error(p.status, kErrFamilyBf16 | kErrRoleMma);
                         ok = false;
@@ -487,7 +515,7 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                         for (int h = 0; h < MH; ++h) {
                             const uint64_t adesc = smem_desc_sw128(a_addr + h * kAHalfBytes + ks * kUmmaK * 2, 16, 1024);
                             mma_f16_ss(d_tmem + static_cast<uint32_t>(h * BN), adesc, bdesc, kIdesc,
-                                       (kb | ks) != 0 ? 1u : 0u);
+                                       (pc.from_partial || kb != pc.s_begin || ks != 0) ? 1u : 0u);
                         }
                     }
                     mma_commit(ring.empty_bar(f)); // stage free once these MMAs have read it
@@ -513,11 +541,47 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
         // its warp index allows) of half h.
         const int quarter = warp & 3;
         const int half = (warp - R::kEpiWarp0) / 4;
-        const uint32_t staging = staging0 + static_cast<uint32_t>(warp - R::kEpiWarp0) * kStagingBytes;
-        int local = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+        const int epi = warp - R::kEpiWarp0;
+        const uint32_t staging = staging0 + static_cast<uint32_t>(epi) * kStagingBytes;
+        // This warp's 32 rows x 256 columns of a hand-over slot, laid out so
+        // that each warp-wide 16-byte access is 512 contiguous bytes.
+        constexpr int kWarpQuads = 32 * BN / 4;
+        for (int local = 0; local < pieces; ++local) {
+            const F32Piece pc = work.piece(local);
             const int slot = local % T::kAccBufs;
             const uint32_t use_parity = static_cast<uint32_t>((local / T::kAccBufs) & 1);
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>((slot * MH + half) * BN);
+            if (pc.from_partial) {
+                // The slot is free (this warp drained its previous use); put
+                // the previous CTA's accumulators there once its flag is up.
+                const bool got = flag_wait_bounded(handover_flags + (cta - 1), p.epoch, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0)
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleHandover);
+                    break;
+                }
+                const uint4 *src = handover_slots + static_cast<size_t>(cta - 1) * kHandoverQuads +
+                                   static_cast<size_t>(epi) * kWarpQuads;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 v = __ldcg(src + (c * 8 + j) * 32 + lane);
+                        r[4 * j] = v.x;
+                        r[4 * j + 1] = v.y;
+                        r[4 * j + 2] = v.z;
+                        r[4 * j + 3] = v.w;
+                    }
+                    tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), r);
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acc_loaded);
+            }
             const bool ok = mbar_wait_bounded(tmem_full0 + 8u * slot, use_parity, p.wait_limit_ns);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0)
@@ -525,12 +589,45 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
+            if (pc.to_partial) {
+                // A head: the next CTA finishes this tile from these
+                // accumulators.  All 256 columns and rows move, in or out of
+                // the matrix.
+                uint4 *dst = handover_slots + static_cast<size_t>(cta) * kHandoverQuads +
+                             static_cast<size_t>(epi) * kWarpQuads;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(dst + (c * 8 + j) * 32 + lane,
+                               make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+                }
+                __threadfence();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(handover_written);
+                    mbar_arrive(tmem_empty0 + 8u * slot);
+                }
+                if (epi == 0 && lane == 0) {
+                    // Every epilogue warp's part is written: raise the flag.
+                    if (mbar_wait_bounded(handover_written, 0, p.wait_limit_ns)) {
+                        __threadfence();
+                        if (!p.withhold_handover) // test hook: the successor must give up
+                            st_release_gpu_u64(handover_flags + cta, p.epoch);
+                    } else {
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleHandover);
+                    }
+                }
+                continue;
+            }
             int mb, nb;
-            tile_coords<MH>(t, tiles_m, tiles_n, mb, nb);
+            tile_coords<MH>(pc.tile, tiles_m, tiles_n, mb, nb);
             const int row0 = mb * BM + half * kUmmaM + quarter * 32; // first row of this warp's box
             const int row = row0 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>((slot * MH + half) * BN);
             float *crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll 1
             for (int c = 0; c < BN / kEpiBoxCols; ++c) {

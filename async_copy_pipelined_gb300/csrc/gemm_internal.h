@@ -61,6 +61,13 @@ struct Bf16Args {
     int num_sms;
     int device;
     unsigned long long ctx;
+    // K split of the last round of tiles (TMA fill; gemm_bf16_ws), as for
+    // the FP32 persistent kernel: hand-over space (nullptr: no split), the
+    // bytes a split of this call needs, this call's flag value, test hook.
+    void *handover;
+    long long handover_bytes;
+    unsigned long long epoch;
+    int withhold_handover;
 };
 
 constexpr int kMaxDevices = 64;

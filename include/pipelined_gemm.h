@@ -152,10 +152,11 @@ typedef struct gemm_plan {
     int grid_y;          /* CTAs launched along y                                      */
     int k_slices;        /* ceil(K / block_k)                                          */
     int options;         /* the GEMM_OPT_* bits the call carries                       */
-    int persistent_ctas; /* CTAs of the split-region kernel gemm_f32_ws would add (one
-                            per SM, each walking several tile pieces), or 0          */
-    int workspace_bytes; /* device workspace gemm_f32_ws can use to split the last round
-                            of tiles in K (0: this call has nothing to split)          */
+    int persistent_ctas; /* FP32: CTAs of the split-region kernel gemm_f32_ws would add
+                            (one per SM, each walking several tile pieces), or 0;
+                            BF16: CTAs of the persistent kernel                      */
+    int workspace_bytes; /* device workspace gemm_f32_ws / gemm_bf16_ws can use to split
+                            the last round of tiles in K (0: nothing to split)         */
 } gemm_plan;
 
 /*
@@ -393,6 +394,45 @@ int gemm_bf16(int M, int N, int K,
               float *C, int ldc,
               int fill_mode, int stages, int block_m,
               void *stream);
+
+/*
+ * gemm_bf16_ws: gemm_bf16 with hand-over space for the TMA fill's K split of
+ * the last round of tiles, as gemm_f32_ws does for FP32.  When the tile
+ * count is not a multiple of the SM count, the persistent CTAs share the
+ * last round and one more as equal runs of 64-deep K blocks; a tile cut
+ * between two CTAs is computed in K order, the second continuing from the
+ * first one's FP32 accumulators, which cross through `workspace` (read
+ * back into tensor memory), so the tensor cores issue the same MMAs on the
+ * same accumulator values as without the split: every result bit is
+ * unchanged.
+ *
+ *   workspace, workspace_bytes
+ *               device memory of at least gemm_plan.workspace_bytes
+ *               (gemm_bf16_plan; one block_m x 256 FP32 tile and an 8-byte
+ *               flag per SM, 0 when the call has nothing to split), 16-byte
+ *               aligned, owned by the caller; nothing in it needs clearing.
+ *               NULL (or a call with nothing to split, or a fill other than
+ *               TMA) runs without the split.
+ *
+ * Calls that overlap on the GPU must not share a workspace.  Returns as
+ * gemm_bf16, plus GEMM_ERR_INVALID_ARG for a workspace smaller than the plan
+ * asks and GEMM_ERR_MISALIGNED for a misaligned one.
+ *
+ * Unlike the FP32 split, this one does not pay on GB300 at 8192^3: each
+ * split tile adds an accumulator drain to global memory and a load back
+ * into tensor memory that the MMAs wait for, and on the 256-row tile (whose
+ * epilogue does not overlap the next tile's MMAs) that costs more than the
+ * idle SMs of the partial last round (603 against 584 us; 128-row tile 647
+ * against 651 us; 4096 x 4096 x 8192, 128 rows: 181 against 191 us).
+ * gemm_bf16 therefore runs without it.
+ */
+int gemm_bf16_ws(int M, int N, int K,
+                 const uint16_t *A, int lda,
+                 const uint16_t *B, int ldb,
+                 float *C, int ldc,
+                 int fill_mode, int stages, int block_m,
+                 void *workspace, size_t workspace_bytes,
+                 void *stream);
 
 /* gemm_bf16_plan: validate exactly as gemm_bf16 does and describe the launch
  * it would make.  With block_m = 0 it asks the current device for its SM
