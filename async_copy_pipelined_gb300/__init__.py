@@ -158,6 +158,8 @@ def _matrix_args(x, name):
     """(rows, cols, ld, pointer) of a 2-D tensor whose rows are contiguous."""
     if x.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
+    if x.numel() == 0:  # an empty matrix has no layout to check (its strides are arbitrary)
+        return x.shape[0], x.shape[1], max(x.shape[1], 1), x.data_ptr()
     if x.shape[1] > 1 and x.stride(1) != 1:
         raise ValueError(f"{name} must have unit column stride (row-major rows)")
     rows, cols = x.shape

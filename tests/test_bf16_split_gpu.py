@@ -115,7 +115,7 @@ def test_handover_wait_times_out_then_exact():
     try:
         import torch
         C = torch.empty((M, N), device="cuda")
-        pg.gemm_bf16(to_device(A, K), to_device(B, N), C, fill="tma", block_m=256)
+        pg.gemm_bf16(to_device(A, K), to_device(B, N), C, fill="tma", block_m=256, workspace="auto")
         st, detail = pg.device_status()
     finally:
         pg.lib().gemm_testing_withhold_handover(0)

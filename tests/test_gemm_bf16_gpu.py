@@ -215,3 +215,26 @@ def test_randomized_shapes(fill, stages, block_m):
         got, _ = run_bf16(A, B, M, N, K, stages=stages, fill=fill, block_m=block_m)
         want = oracle.gemm_bf16_f64(A, B, M, N, K)
         _check(got, want, _abs_products(A, B, M, N, K), K, f"bf16 {fill} S{stages} T{block_m} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fill", ["tma", "cpasync"])
+def test_host_tensors_chunked_match_device_path(fill):
+    """BF16 host tensors: B first, then row chunks of A in, GEMM, rows of C
+    out on three streams; the same bits as one device call, and within the
+    float32-accumulation bound of the oracle."""
+    import torch
+    import async_copy_pipelined_gb300 as pg
+    M, N, K = 2000, 4096, 136
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunks = pg.host_row_chunks(M, N, sms)
+    assert len(chunks) > 1 and chunks[-1][1] == M
+    A, B = bf16_operands("normal", M, N, K, 91)
+    Ah = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()[:, :K]
+    Bh = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).pin_memory()[:, :N]
+    Ch = pg.gemm_bf16(Ah, Bh, fill=fill)
+    assert not Ch.is_cuda
+    got, _ = run_bf16(A, B, M, N, K, fill=fill)
+    np.testing.assert_array_equal(Ch.numpy().view(np.uint32), got.view(np.uint32))
+    rows = sample_rows(M, 24, 92)
+    want = oracle_bf16_rows(A, B, rows, N, K)
+    _check(Ch.numpy()[rows], want, _abs_products(A[rows], B, len(rows), N, K), K, f"bf16 host path {fill}")
