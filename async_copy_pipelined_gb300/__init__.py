@@ -317,7 +317,7 @@ def _f32_host_call(A, B, C, code, stages, block_tile):
     _check(st, "gemm_f32_host")
     # The executor copied the status word out after its last GEMM: a kernel
     # that gave up on a bounded wait left its rows of C undefined.
-    detail = int(word[0]) & 0xFFFFFFFF
+    detail = ctypes.c_uint32.from_address(word.data_ptr()).value
     if detail:
         _check(GEMM_ERR_TIMEOUT, f"host-buffer GEMM (device status word {detail:#x})")
     return C
