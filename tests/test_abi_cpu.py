@@ -375,3 +375,20 @@ def test_producer_warp_fill_plan(lib):
     with pytest.raises(pg.GemmError) as e:
         pg.plan_bf16(256, 256, 256, fill="cpasync_ws")
     assert e.value.status == 3
+
+
+def test_bf16_plan_split_workspace():
+    """The BF16 TMA fill offers the K split of the last round where the
+    persistent CTAs (152 without a device) leave a partial round and a tile
+    has at least two K blocks: one block_m x 256 FP32 slot and an 8-byte
+    flag per CTA.  Other fills, whole rounds and single-block K offer none."""
+    for block_m in (128, 256):
+        p = pg.plan_bf16(4352, 2304, 512, fill="tma", block_m=block_m)
+        assert p["workspace_bytes"] == 152 * (block_m * 256 * 4 + 8)
+        assert p["persistent_ctas"] == 152
+        assert pg.plan_bf16(4352, 2304, 512, fill="cpasync", block_m=block_m)["workspace_bytes"] == 0
+        assert pg.plan_bf16(4352, 2304, 512, fill="sync", block_m=block_m)["workspace_bytes"] == 0
+        assert pg.plan_bf16(4352, 2304, 64, fill="tma", block_m=block_m)["workspace_bytes"] == 0  # one K block
+    assert pg.plan_bf16(8192, 8192, 8192, fill="tma", block_m=256)["workspace_bytes"] == 152 * (256 * 256 * 4 + 8)
+    # 19 x 8 = 152 tiles of 256 rows: one whole round, nothing to split
+    assert pg.plan_bf16(19 * 256, 8 * 256, 512, fill="tma", block_m=256)["workspace_bytes"] == 0
