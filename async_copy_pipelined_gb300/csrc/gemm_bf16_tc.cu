@@ -492,10 +492,15 @@ __global__ void __launch_bounds__(bf16::Roles<Fill, MH>::kThreads, 1)
                     break;
                 }
                 // A tail continues from the accumulators the epilogue warps
-                // have put into this slot.
-                if (pc.from_partial && !mbar_wait_bounded(acc_loaded, 0, p.wait_limit_ns)) {
-                    record_error(p.status, kErrFamilyBf16 | kErrRoleHandover);
-                    break;
+                // have put into this slot.  Every epilogue warp has then seen
+                // the previous CTA's flag, so it goes back to 0 (as in the
+                // FP32 split: a replayed call cannot mistake it for new).
+                if (pc.from_partial) {
+                    if (!mbar_wait_bounded(acc_loaded, 0, p.wait_limit_ns)) {
+                        record_error(p.status, kErrFamilyBf16 | kErrRoleHandover);
+                        break;
+                    }
+                    st_release_gpu_u64(handover_flags + (cta - 1), 0ull);
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * MH * BN);

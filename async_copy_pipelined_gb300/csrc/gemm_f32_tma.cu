@@ -159,8 +159,12 @@ __global__ void __launch_bounds__(T::kThreads + 32, T::kMinBlocksTma)
 // Consumers: wait until the previous CTA has raised its hand-over flag.  One
 // thread polls the flag (bounded) and arrives on `received`; the others wait
 // on `received` (bounded), so a warp that has already given up strands no
-// one.  True when the accumulators may be read.
-__device__ __noinline__ bool f32_handover_wait(const unsigned long long *flag, unsigned long long epoch,
+// one.  True when the accumulators may be read.  The polling thread, the
+// flag's only reader, lowers it again once it has seen it: every flag a call
+// raises is back at 0 when the call ends, so a call replayed with the same
+// flag value (a captured CUDA graph) cannot mistake an old flag for a new
+// one.
+__device__ __noinline__ bool f32_handover_wait(unsigned long long *flag, unsigned long long epoch,
                                                uint64_t limit_ns, unsigned int *status, uint32_t received,
                                                volatile int *failed)
 {
@@ -169,6 +173,8 @@ __device__ __noinline__ bool f32_handover_wait(const unsigned long long *flag, u
         *failed = flag_wait_bounded(flag, epoch, limit_ns) ? 0 : 1;
         if (*failed)
             record_error(status, kErrFamilyF32Tma | kErrRoleHandover);
+        else
+            st_release_gpu_u64(flag, 0ull);
         mbar_arrive(received); // releases *failed to the other warps
     }
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(received, 0, limit_ns))) {

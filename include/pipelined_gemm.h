@@ -231,6 +231,14 @@ int gemm_f32(int M, int N, int K,
  * start in index order, so the one it waits for is running or done.  If
  * the wait expires, GEMM_ERR_TIMEOUT is recorded (role 6) as for any wait.
  * Other arguments, errors and ownership as gemm_f32.
+ *
+ * CUDA graphs: a hand-over's ready flag carries a value fixed when the call
+ * is made, which a captured graph replays unchanged; each flag's one reader
+ * lowers it to 0 once it has seen it, so a call that completes leaves every
+ * flag at 0 and a replay waits for its own hand-overs.  A call that ended
+ * with GEMM_ERR_TIMEOUT may leave a flag raised: clear the workspace's flags
+ * (the last ctas x 8 bytes of plan.workspace_bytes) before replaying a graph
+ * that uses it.  The same holds for gemm_bf16_ws.
  */
 int gemm_f32_ws(int M, int N, int K,
                 const float *A, int lda,
