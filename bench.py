@@ -390,9 +390,19 @@ class GemmCall:
         return self.fn()
 
 
-def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, options=(), workspace="auto"):
+_LIBRARY_DEFAULT = object()
+
+
+def gemm_call(pg, name, Ad, Bd, Cd, fill, stages, tile, options=(), workspace=_LIBRARY_DEFAULT):
+    """A call of the binding as a user makes it; `workspace` as the binding
+    takes it, by default the binding's own default (FP32: "auto", the K
+    split; BF16: None, no split)."""
     if name.startswith("bf16"):
-        return GemmCall(lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile, options=options), 1)
+        ws = None if workspace is _LIBRARY_DEFAULT else workspace
+        return GemmCall(lambda: pg.gemm_bf16(Ad, Bd, Cd, fill=fill, stages=stages, block_m=tile, options=options,
+                                             workspace=ws), 1)
+    if workspace is _LIBRARY_DEFAULT:
+        workspace = "auto"
     k = f32_kernels_per_call(pg, Ad.shape[0], Bd.shape[1], Ad.shape[1], Ad.stride(0), Bd.stride(0), fill, stages,
                              tile, workspace)
     return GemmCall(lambda: pg.gemm_f32(Ad, Bd, Cd, fill=fill, stages=stages, block_tile=tile, options=options,
@@ -811,6 +821,28 @@ def run_ours(args, dist: Dist):
             for v in bfills.values():
                 v["t_sync_over_t"] = bfills["sync/S1/T128"]["ms"] / v["ms"]
             extras["bf16_8192"]["fills"] = bfills
+            # The TMA fill's opt-in K split of the last round (gemm_bf16_ws)
+            # against the default unsplit call, both tiles; bits checked equal.
+            bsplit = {}
+            for t in (256, 128):
+                pb_t = pg.plan_bf16(wb["M"], wb["N"], wb["K"], lda=wb["lda"], fill="tma", block_m=t)
+                ref = None
+                for label, ws in (("unsplit", None), ("split", "auto")):
+                    c = gemm_call(pg, "bf16_8192", Abd, Bbd, Cbd, "tma", pb_t["stages"], t, workspace=ws)
+                    c()
+                    _count(c, 1)
+                    torch.cuda.synchronize()
+                    check_status(pg, f"BF16 {label} T{t}")
+                    same = True
+                    if ref is None:
+                        ref = Cbd.clone()
+                    else:
+                        same = bool(torch.equal(Cbd.view(torch.int32), ref.view(torch.int32)))
+                    m2, b2, md2 = time_kernel(pg, c, flush, args.sweep_launches)
+                    bsplit[f"tma/S{pb_t['stages']}/T{t}/{label}"] = {"tflops": fb / (m2 / 1e3) / 1e12, "ms": m2,
+                                                                    "ms_min": b2, "bits_equal_unsplit": same}
+                del ref
+            extras["bf16_8192"]["k_split"] = bsplit
             co, n = time_cache_options(pg, "bf16_8192", Abd, Bbd, Cbd, [("tma", 3, 256), ("cpasync", 3, 256)], flush,
                                        args.sweep_launches, fb)
             extras["cache_options_bf16_8192"] = co
