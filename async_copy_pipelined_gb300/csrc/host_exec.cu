@@ -321,8 +321,6 @@ extern "C" int gemm_f32_host(int M, int N, int K, const float *A, int lda, const
 {
     if ((fill_mode & GEMM_OPT_ACCUMULATE) != 0)
         return GEMM_ERR_INVALID_ARG; // this entry computes C = A·B; it uses the option itself
-    // The whole problem decides the tile, and its plan validates everything
-    // the chunk calls will be given.
     // Host operands: any row pitch at least their width, 4-byte aligned.
     if (M < 0 || N < 0 || K < 0 || lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
         return GEMM_ERR_INVALID_ARG;
