@@ -36,7 +36,8 @@ constexpr int kDefaultStagesF32 = 4;
 // in flight while one is computed.
 constexpr int kDefaultStagesF32TmaTile128 = 2;
 // The producer-warp cp.async fill runs best with two (GB300, 4096^3,
-// TFLOP/s for 2 / 3 / 4 / 6 stages: 57.8 / 56.4 / 55.4 / 56.6).
+// TFLOP/s for 2 / 3 / 4 stages with four producer warps: 58.1 / 57.3 /
+// 57.3).
 constexpr int kDefaultStagesF32CpAsyncWs = 2;
 // BF16 ring depth: four 48 KiB stages for the 128-row tile, three 64 KiB
 // stages for the 256-row tile (four of those do not fit in 227 KiB).

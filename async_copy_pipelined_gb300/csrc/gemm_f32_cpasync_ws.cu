@@ -3,8 +3,8 @@
 //
 // "A study on CUDA async memcpy" closes its block-scoped pipeline with the
 // remark that producers and consumers need not be the same threads: a few
-// warps can fill the stages while the rest only compute.  Here one or two
-// producer warps (one for the 64x64 and 32x32 tiles, two for 128x128) issue
+// warps can fill the stages while the rest only compute.  Here one or four
+// producer warps (one for the 64x64 and 32x32 tiles, four for 128x128) issue
 // every 16-byte cp.async of a slice, each thread then arranging with
 // cp.async.mbarrier.arrive.noinc that the stage's full barrier (count: the
 // producer threads) completes once its copies have landed.  The consumers
@@ -22,8 +22,13 @@
 
 namespace pg {
 
+// Producer threads: four warps on the 128x128 tile (GB300, 4096^3, TFLOP/s
+// for 2 / 3 / 4 stages with one, two and four producer warps: 57.2 / 57.0 /
+// 56.8, 57.9 / 56.5 / 55.5, 58.1 / 57.3 / 57.3; 3000 x 5000 x 1000 at two
+// stages 42.3, 48.5, 49.4); one on the smaller tiles, whose three CTAs per
+// SM leave no registers for more.
 template <class T>
-constexpr int ws_producer_threads() { return T::kThreads >= 256 && T::BM == 128 ? 64 : 32; }
+constexpr int ws_producer_threads() { return T::kThreads >= 256 && T::BM == 128 ? 128 : 32; }
 
 template <class T>
 constexpr int ws_threads() { return T::kThreads + ws_producer_threads<T>(); }

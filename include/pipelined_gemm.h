@@ -28,7 +28,7 @@
  *                      copies and computes; no CTA barrier in the loop.
  *   GEMM_FILL_CPASYNC_WS
  *                      the same cp.async copies and mbarrier completion,
- *                      issued by one or two dedicated producer warps while
+ *                      issued by one or four dedicated producer warps while
  *                      the other warps only compute ("A study on CUDA async
  *                      memcpy", "block-scoped pipeline": producers and
  *                      consumers need not be the same threads).  FP32 only.

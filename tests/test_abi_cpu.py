@@ -365,11 +365,11 @@ def test_cache_policy_refused_on_four_byte_copies(lib):
 
 
 def test_producer_warp_fill_plan(lib):
-    """The producer-warp cp.async fill: eight consumer warps plus two producer
+    """The producer-warp cp.async fill: eight consumer warps plus four producer
     warps on the 128 tile (one on the 64 and 32 tiles), two stages by
     default, 16-byte copies; refused for the tensor-core GEMM."""
     p = pg.plan_f32(4096, 4096, 4096, fill="cpasync_ws")
-    assert p["threads"] == 320 and p["stages"] == 2 and p["a_copy_bytes"] == 16
+    assert p["threads"] == 384 and p["stages"] == 2 and p["a_copy_bytes"] == 16
     assert pg.plan_f32(1024, 1024, 1024, fill="cpasync_ws", stages=3)["threads"] == 288
     assert pg.plan_f32(32, 32, 65536, fill="cpasync_ws", block_tile=32)["threads"] == 64
     with pytest.raises(pg.GemmError) as e:
