@@ -596,7 +596,7 @@ using namespace pg;
 // ================================================================ C ABI
 extern "C" {
 
-int gemm_version(void) { return 10000; }
+int gemm_version(void) { return 10100; }
 
 const char *gemm_status_string(int status)
 {
