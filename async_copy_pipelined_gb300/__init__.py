@@ -54,7 +54,7 @@ class GemmPlan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "fill_mode", "block_m", "block_n", "block_k", "thread_m", "thread_n", "threads", "stages",
         "a_copy_bytes", "b_copy_bytes", "smem_bytes", "grid_x", "grid_y", "k_slices", "options",
-        "persistent_ctas", "workspace_bytes")]
+        "persistent_ctas", "workspace_bytes", "wide_rows")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -95,6 +95,10 @@ def _bind(l):
     l.gemm_testing_set_hooks.restype = I
     l.gemm_testing_withhold_handover.argtypes = [I]
     l.gemm_testing_withhold_handover.restype = I
+    l.gemm_testing_f32_wide.argtypes = [I]
+    l.gemm_testing_f32_wide.restype = I
+    l.gemm_testing_f32_wide_rows.argtypes = [I, I, I, I, I]
+    l.gemm_testing_f32_wide_rows.restype = I
     l.gemm_testing_f32_piece.argtypes = [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)]
     l.gemm_testing_f32_piece.restype = I
     l.gemm_f32_host.argtypes = [I, I, I, P, I, P, I, P, I, I, I, I, P, ctypes.c_size_t, P, P]
@@ -548,3 +552,19 @@ def testing_set_hooks(wait_limit_ns: int = 0, withhold: int = -1) -> None:
     limit (0: the default 2 s) and a ring position their producers leave
     unfilled (-1: none), for every later call in this process."""
     _check(lib().gemm_testing_set_hooks(int(wait_limit_ns), int(withhold)), "gemm_testing_set_hooks")
+
+
+def testing_f32_wide(mode: int = -1) -> None:
+    """How later FP32 TMA calls on the 128 tile pick their wide rows
+    (include/pipelined_gemm_testing.h): -1 by the cost model, 0 never,
+    1 whenever a cut exists.  The bits are the same in every mode."""
+    _check(lib().gemm_testing_f32_wide(int(mode)), "gemm_testing_f32_wide")
+
+
+def f32_wide_rows(M: int, N: int, K: int, sms: int = 152, mode: int = -1) -> int:
+    """Rows [0, r) of an M x N x K TMA call on the 128 tile that the
+    128 x 256 wide-row kernel computes (computed on the host)."""
+    r = lib().gemm_testing_f32_wide_rows(int(M), int(N), int(K), int(sms), int(mode))
+    if r < 0:
+        raise ValueError("invalid arguments")
+    return r

@@ -74,6 +74,7 @@ static std::atomic<int> g_num_sms[kMaxDevices];
 static std::atomic<unsigned long long> g_hook_wait_limit_ns{0}; // 0: kDefaultWaitLimitNs
 static std::atomic<int> g_hook_withhold{-1};
 static std::atomic<int> g_hook_withhold_handover{0};
+static std::atomic<int> g_hook_f32_wide{-1}; // f32_wide_rows mode: -1 model, 0 off, 1 forced
 
 // Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
 // if the driver cannot say.  Per-context state (the status word's address,
@@ -382,17 +383,27 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
     // The TMA fill's 128 x 128 tile: with hand-over space (gemm_f32_ws) and
     // a tile count that is not a multiple of the SM count, the last round
     // and one more are split in K over one CTA per SM (f32_schedule.cuh).
+    //
+    // Before that, the top rows may go to the wide-row kernel (128 x 256
+    // tiles, gemm_f32_tma_wide.cu) where it shortens the call; the 128 x 128
+    // path, split included, then covers the rows below them.  Plain copies
+    // only: the wide kernel carries no cache qualifiers.
     int ctas = 0;
     long long handover = 0;
     int region0 = 0x7fffffff;
+    int wide_rows = 0;
     if (fill == GEMM_FILL_TMA && tile == 128 && work && K > 0) {
-        const long long tiles = grid_x * grid_y;
         const int sms = planning_sms();
-        const F32Schedule sch = F32Schedule::make(static_cast<int>(tiles), sms, (K + 15) / 16, true);
-        if (sch.split()) {
-            ctas = sms;
-            handover = f32_handover_bytes(sms);
-            region0 = sch.region0;
+        if (copy_form == 0 && pol_a == 0 && pol_b == 0)
+            wide_rows = f32_wide_rows(M, N, K, sms, g_hook_f32_wide.load());
+        const long long tiles = grid_x * ((M - wide_rows + tile - 1) / tile);
+        if (tiles > 0) {
+            const F32Schedule sch = F32Schedule::make(static_cast<int>(tiles), sms, (K + 15) / 16, true);
+            if (sch.split()) {
+                ctas = sms;
+                handover = f32_handover_bytes(sms);
+                region0 = sch.region0;
+            }
         }
     }
 
@@ -420,6 +431,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         plan->options = fill_mode & GEMM_OPT_MASK;
         plan->persistent_ctas = ctas;
         plan->workspace_bytes = static_cast<int>(handover);
+        plan->wide_rows = wide_rows;
     }
     if (args) {
         args->M = M;
@@ -444,6 +456,7 @@ static int plan_f32(int M, int N, int K, const float *A, int lda, const float *B
         args->pol_a = pol_a;
         args->pol_b = pol_b;
         args->ctas = 0;         // set when the call brings hand-over space
+        args->wide_rows = wide_rows;
         args->tile_limit = 0x7fffffff;
         args->split_ctas = ctas;
         args->split_region0 = region0;
@@ -596,7 +609,7 @@ using namespace pg;
 // ================================================================ C ABI
 extern "C" {
 
-int gemm_version(void) { return 10100; }
+int gemm_version(void) { return 10200; }
 
 const char *gemm_status_string(int status)
 {
@@ -662,8 +675,21 @@ int gemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, in
     case GEMM_FILL_CPASYNC: return launch_f32_cpasync(args, s);
     case GEMM_FILL_CPASYNC_MBAR: return launch_f32_cpasync_mbar(args, s);
     case GEMM_FILL_CPASYNC_WS: return launch_f32_cpasync_ws(args, s);
-    default: return launch_f32_tma(args, s);
+    default: break;
     }
+    if (args.wide_rows > 0) {
+        // Rows [0, wide_rows) on 128 x 256 tiles, then the rest on the
+        // 128 x 128 path, in that order on the stream (disjoint rows of C).
+        F32Args wide = args;
+        wide.M = args.wide_rows;
+        st = launch_f32_tma_wide(wide, s);
+        if (st != GEMM_OK || args.wide_rows == M)
+            return st;
+        args.A += static_cast<long long>(args.wide_rows) * args.lda;
+        args.C += static_cast<long long>(args.wide_rows) * args.ldc;
+        args.M = M - args.wide_rows;
+    }
+    return launch_f32_tma(args, s);
 }
 
 int gemm_bf16_plan(int M, int N, int K, const uint16_t *A, int lda, const uint16_t *B, int ldb, float *C, int ldc,
@@ -766,6 +792,21 @@ int gemm_testing_f32_piece(int tiles, int ctas, int k_slices, int split, int cta
     out[3] = pc.from_partial ? 1 : 0;
     out[4] = pc.to_partial ? 1 : 0;
     return 1;
+}
+
+int gemm_testing_f32_wide(int mode)
+{
+    if (mode < -1 || mode > 1)
+        return GEMM_ERR_INVALID_ARG;
+    g_hook_f32_wide.store(mode);
+    return GEMM_OK;
+}
+
+int gemm_testing_f32_wide_rows(int M, int N, int K, int sms, int mode)
+{
+    if (M < 0 || N < 0 || K < 0 || sms < 1 || mode < -1 || mode > 1)
+        return -1;
+    return f32_wide_rows(M, N, K, sms, mode);
 }
 
 int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position)

@@ -30,6 +30,7 @@ struct F32Args {
     int withhold;          // ring position a producer leaves unfilled (test hook; -1: none)
     int copy_form;         // cp.async qualifiers: bit 0 .L2::128B prefetch, bit 1 .L2::cache_hint
     int pol_a, pol_b;      // L2 policy per operand: 0 normal, 1 evict_first, 2 evict_last
+    int wide_rows;         // TMA fill, 128 tile: rows [0, wide_rows) go to the wide-row kernel (0: none)
     int tile_limit;        // one-tile TMA kernel: CTAs of linear tile index >= this exit at once
     int ctas;              // split-region TMA kernel: CTAs launched (0: no split)
     int split_ctas;        // what a split would use (planning; 0: nothing to split)
@@ -92,6 +93,16 @@ int ensure_smem_limit(Kernel kernel, int smem, int dev, unsigned long long ctx,
 int launch_f32_sync(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync(const F32Args &a, cudaStream_t s);
 int launch_f32_tma(const F32Args &a, cudaStream_t s);
+// The TMA fill's wide-row kernel (128 x 256 tiles, gemm_f32_tma_wide.cu) on
+// rows [0, a.M): the caller passes a.M = the wide rows.
+int launch_f32_tma_wide(const F32Args &a, cudaStream_t s);
+// Rows of an M x N x K TMA call on the 128 tile that the wide-row kernel
+// takes (a multiple of 128, or M), chosen by its measured round times;
+// `mode` -1 decides by the model, 0 never, 1 whenever some cut is possible.
+int f32_wide_rows(int M, int N, int K, int sms, int mode);
+constexpr int kF32WideStages = 4;       // the wide-row kernel's ring (measured best of 2, 3, 4)
+constexpr int kF32WideMinK = 1024;      // shorter K stays on the 128 x 128 tile
+int f32_wide_smem_bytes();
 int launch_f32_cpasync_mbar(const F32Args &a, cudaStream_t s);
 int launch_f32_cpasync_ws(const F32Args &a, cudaStream_t s);
 int f32_cpasync_ws_threads(int tile);
@@ -132,6 +143,7 @@ constexpr unsigned int kErrFamilyBf16 = 2;
 constexpr unsigned int kErrFamilySelftest = 3;
 constexpr unsigned int kErrFamilyF32CpAsyncMbar = 4;
 constexpr unsigned int kErrFamilyF32CpAsyncWs = 5;
+constexpr unsigned int kErrFamilyF32TmaWide = 6;
 constexpr unsigned int kErrRoleConsumer = 1u << 8;
 constexpr unsigned int kErrRoleProducer = 2u << 8;
 constexpr unsigned int kErrRoleMma = 3u << 8;

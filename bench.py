@@ -366,17 +366,25 @@ def to_device(x, cols, dev):
 
 
 def f32_kernels_per_call(pg, M, N, K, lda, ldb, fill, stages, tile, workspace="auto") -> int:
-    """Kernel launches one device-buffer FP32 call makes: the TMA fill with a
-    hand-over workspace splits the last round of 128 x 128 tiles in K, which
-    takes the one-tile kernel for the whole rounds before it (if any) and the
-    persistent kernel for the split region; every other call is one launch."""
-    if fill != "tma" or workspace is None or M == 0 or N == 0:
+    """Kernel launches one device-buffer FP32 call makes.  The TMA fill on
+    the 128 tile may first run the wide-row kernel on its top rows
+    (plan["wide_rows"]); the rows below it, with a hand-over workspace, split
+    the last round of 128 x 128 tiles in K, which takes the one-tile kernel
+    for the whole rounds before it (if any) and the persistent kernel for the
+    split region.  Every other call is one launch."""
+    if fill != "tma" or M == 0 or N == 0 or K == 0:
         return 1
     p = pg.plan_f32(M, N, K, lda=lda, ldb=ldb, fill=fill, stages=stages, block_tile=tile)
+    wide = p["wide_rows"]
+    n = 1 if wide > 0 else 0
+    rows = M - wide
+    if rows <= 0:
+        return n
     ctas = p["persistent_ctas"]
-    if ctas <= 0:
-        return 1
-    return 2 if (p["grid_x"] * p["grid_y"]) // ctas >= 2 else 1
+    if workspace is None or ctas <= 0:
+        return n + 1
+    tiles = p["grid_x"] * ((rows + p["block_m"] - 1) // p["block_m"])
+    return n + (2 if tiles // ctas >= 2 else 1)
 
 
 class GemmCall:
@@ -721,6 +729,19 @@ def run_ours(args, dist: Dist):
             mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
             fills["tma/S4/T128/unsplit"] = {"tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best,
                                             "ms_median": med, "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
+            # Every row on 128 x 128 tiles (the wide-row kernel switched off
+            # for these calls): same bits.
+            if w["lda"] % 4 == 0:
+                pg.testing_f32_wide(0)
+                try:
+                    for s in (2, 4):
+                        c = gemm_call(pg, name, Ad, Bd, Cd, "tma", s, 128)
+                        mean, best, med = time_kernel(pg, c, flush, args.sweep_launches)
+                        fills[f"tma/S{s}/T128/no-wide"] = {
+                            "tflops": flops / (mean / 1e3) / 1e12, "ms": mean, "ms_min": best, "ms_median": med,
+                            "frac_fp32_peak": flops / (mean / 1e3) / 1e12 / fp32_peak}
+                finally:
+                    pg.testing_f32_wide(-1)
             t_sync = fills["sync/S1/T128"]["ms"]
             for v in fills.values():
                 v["t_sync_over_t"] = t_sync / v["ms"]

@@ -157,6 +157,15 @@ typedef struct gemm_plan {
                             BF16: CTAs of the persistent kernel                      */
     int workspace_bytes; /* device workspace gemm_f32_ws / gemm_bf16_ws can use to split
                             the last round of tiles in K (0: nothing to split)         */
+    int wide_rows;       /* FP32 TMA fill, 128x128 tile: rows [0, wide_rows) of C that
+                            the call computes on 128x256 tiles (8x16 micro-tile, 256
+                            threads, 4 stages, no producer warp) before the 128x128
+                            path computes the rest; 0 when the wide kernel would not
+                            shorten the call (K < 1024, cache options, or no cut in
+                            whole rounds of wide tiles that gains 1 %).  grid_x and
+                            grid_y still count the 128x128 tiles of the whole C;
+                            persistent_ctas and workspace_bytes describe the rows
+                            below wide_rows.  Same bits either way.           */
 } gemm_plan;
 
 /*
@@ -463,7 +472,7 @@ const char *gemm_status_string(int status);
  * GEMM_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives the raw word (0 when clean): bits 0-7 the kernel family
  * (1 FP32 TMA, 2 BF16, 3 self-test, 4 FP32 mbarrier-completed cp.async,
- * 5 FP32 cp.async from producer warps),
+ * 5 FP32 cp.async from producer warps, 6 FP32 TMA wide-row kernel),
  * bits 8-15 the waiting role (1 consumer, 2 producer, 3 MMA issuer,
  * 4 epilogue, 5 drain of copies or MMAs still in flight, 6 hand-over of
  * accumulators between CTAs in gemm_f32_ws).

@@ -28,7 +28,8 @@ extern "C" {
  *   withhold_position  ring position (0, 1, 2, ... counted per CTA over all
  *                      of its K slices, and over its tiles for the
  *                      persistent tensor-core kernel) that the producers of
- *                      the FP32 TMA fill, both FP32 mbarrier-completed
+ *                      the FP32 TMA fill (its wide-row kernel included),
+ *                      both FP32 mbarrier-completed
  *                      cp.async fills and all three BF16 fills leave
  *                      unfilled: no copy is issued and no arrival (and, for
  *                      TMA, no expected-transaction count) is made for it.
@@ -42,6 +43,23 @@ extern "C" {
  * concurrent GEMM calls that expect the defaults.
  */
 int gemm_testing_set_hooks(unsigned long long wait_limit_ns, int withhold_position);
+
+/*
+ * gemm_testing_f32_wide: how later FP32 TMA calls on the 128x128 tile choose
+ * their wide rows (gemm_plan.wide_rows): -1 by the measured cost model (the
+ * default), 0 never (every row on 128x128 tiles), 1 whenever a cut in whole
+ * rounds of 128x256 tiles exists, gain or not.  Results are bit-identical in
+ * every mode.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG.  Not thread-safe
+ * against concurrent calls that expect the default.
+ */
+int gemm_testing_f32_wide(int mode);
+
+/*
+ * gemm_testing_f32_wide_rows: the wide rows an M x N x K call would take on
+ * a device of `sms` SMs in `mode` (as above), computed on the host without a
+ * device; -1 for invalid arguments.
+ */
+int gemm_testing_f32_wide_rows(int M, int N, int K, int sms, int mode);
 
 /*
  * gemm_testing_withhold_handover: with `on` non-zero, every later

@@ -57,7 +57,7 @@ def test_build_targets_sm103a_only():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.gemm_version() == 10100  # 1.1.0
+    assert lib.gemm_version() == 10200  # 1.2.0
     for code in range(7):
         s = pg.status_string(code)
         assert s.startswith("GEMM_")
