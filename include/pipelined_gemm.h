@@ -194,7 +194,10 @@ typedef struct gemm_plan {
  *               threads), 32 (32x32 tile, 8x4 micro-tile, one warp: the
  *               latency-bound shape of "A study on CUDA async memcpy",
  *               "Real world example"), or 0 to let the library choose by
- *               problem size (64 or 128).
+ *               problem size (64 or 128).  With GEMM_FILL_TMA and 128, a
+ *               large call may compute its top rows on 128x256 tiles
+ *               (gemm_plan.wide_rows) before the 128x128 tiles below them;
+ *               the bits are the same.
  *   stream      cudaStream_t to enqueue on.
  *
  * Alignment: the sync and both cp.async fills accept any lda/ldb; rows that are
