@@ -490,7 +490,7 @@ const char *gemm_status_string(int status);
  *     between them by a kernel on another stream is lost, and calls that
  *     overlap on the GPU race on the word: whichever caller reads first
  *     sees (and clears) the other's error.
- * Callers that need a per-call verdict serialise their GEMMs on one stream
+ * Callers that need a status per call serialise their GEMMs on one stream
  * and call gemm_device_status after each.  GEMM results on the device path
  * are only known good once gemm_device_status has returned GEMM_OK for a
  * point after them.
