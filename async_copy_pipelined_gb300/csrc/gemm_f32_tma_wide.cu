@@ -25,11 +25,15 @@
 //
 // Measured on GB300 (probe of this kernel, TFLOP/s, bits equal): one round
 // of 152 tiles, 2432 x 2048 x 4096, 64.9 against 61.8 for the 128 x 128 TMA
-// kernel's two rounds; x 16384 K 65.5 against 62.9; two / three / four stages
-// 62.7 / 64.5 / 64.9.  A tile twice as wide makes half as many tiles, so
-// whole rounds are rarer: f32_wide_rows() gives the kernel the top rows of a
-// call only where that shortens the call, and the 128 x 128 path (with its K
-// split of the last round) computes the rest.
+// kernel's two rounds; x 16384 K 65.5 against 62.9; two / three / four /
+// five / six stages 62.7 / 64.5 / 64.9 / 64.5 / 64.3; A as one LDS.32 per
+// row per k instead of pairs 63.3.  At 4096^3 the call (wide rows 0-2431,
+// then the 128 x 128 path) ran 62.1 against 61.2.
+//
+// A tile twice as wide makes half as many tiles, so whole rounds are rarer:
+// f32_wide_rows() gives the kernel the top rows of a call only where that
+// shortens the call, and the 128 x 128 path (with its K split of the last
+// round) computes the rest.
 #include <numeric>
 
 #include "f32_schedule.cuh"
